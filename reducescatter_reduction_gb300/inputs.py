@@ -1,0 +1,120 @@
+"""Seeded synthetic rank buffers for the collectives' workloads.
+
+This module only draws random numbers and stores them in the element type; it
+holds none of the reduction's arithmetic.  Both the CUDA path's tests/benchmark
+and the CPU oracle's tests take their inputs from here.
+
+Every rank r of a workload with seed s draws from ``numpy.random.default_rng([s, r])``.
+Normals are drawn in float32 and stored as the element type with
+round-to-nearest-even (numpy for fp16, torch's CPU cast for bf16).
+
+Workloads (the shapes of the pages' measurements: nccl-tests style message
+sweeps and tensor-parallel activations, see "MSCCL++" evaluation and T-CCL
+section "Experimental Setup"):
+
+============  =========================================================  ======
+name          buffers                                                    seed
+============  =========================================================  ======
+worked        p=2, n=4096 fp32, uniform ints in [-8, 8]; elements 0..3   1
+              of ranks 0/1 are the all-reduce worked example
+sweep         p=8 bf16, n = 2^9 .. 2^27 per rank (1 KiB .. 256 MiB), N(0,1)  2
+tp            p=8 bf16, [tokens, 8192], tokens in {1, 32, 256, 4096},    3
+              N(0, 0.02)
+coverage      p=8, n = 64 Mi; int32 uniform in [-1000, 1000] (prod: values  4
+              from {-1, 1, 2}); fp32 / fp16 N(0, 1)
+moe           p=16 bf16, [16384, 7168] per rank, N(0, 1)                 5
+============  =========================================================  ======
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# element storage: fp16 and bf16 are kept as raw 16-bit patterns
+STORAGE = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16, "i32": np.int32}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "i32": 4}
+
+SEEDS = {"worked": 1, "sweep": 2, "tp": 3, "coverage": 4, "moe": 5}
+
+# The all-reduce worked example ("Inside NCCL AllReduce", "What all-reduce promises").
+WORKED_A = [8.0, 0.0, 4.0, 2.0]
+WORKED_B = [0.0, 4.0, 8.0, 6.0]
+
+SWEEP_N = [1 << k for k in range(9, 28)]        # bf16 elements per rank: 1 KiB .. 256 MiB
+TP_HIDDEN = 8192
+TP_TOKENS = [1, 32, 256, 4096]
+COVERAGE_N = 64 * 1024 * 1024
+MOE_SHAPE = (16384, 7168)
+
+
+def rng(seed: int, rank: int) -> np.random.Generator:
+    return np.random.default_rng([seed, rank])
+
+
+def store(vals_f32: np.ndarray, dtype: str) -> np.ndarray:
+    """Store float32 values as the element type (RNE), returning raw storage."""
+    vals_f32 = np.ascontiguousarray(vals_f32, dtype=np.float32)
+    if dtype == "f32":
+        return vals_f32
+    if dtype == "f16":
+        return vals_f32.astype(np.float16).view(np.uint16)
+    if dtype == "bf16":
+        import torch
+        t = torch.from_numpy(vals_f32).to(torch.bfloat16)
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    if dtype == "i32":
+        return vals_f32.astype(np.int32)
+    raise ValueError(dtype)
+
+
+def normal(n: int, seed: int, rank: int, sigma: float, dtype: str) -> np.ndarray:
+    v = rng(seed, rank).standard_normal(n, dtype=np.float32)
+    if sigma != 1.0:
+        v *= np.float32(sigma)
+    return store(v, dtype)
+
+
+def uniform_int(n: int, seed: int, rank: int, lo: int, hi: int, dtype: str) -> np.ndarray:
+    v = rng(seed, rank).integers(lo, hi + 1, size=n, dtype=np.int32)
+    if dtype == "i32":
+        return v
+    return store(v.astype(np.float32), dtype)
+
+
+def choice(n: int, seed: int, rank: int, values, dtype: str) -> np.ndarray:
+    vals = np.asarray(values, dtype=np.int32)
+    v = vals[rng(seed, rank).integers(0, len(vals), size=n)]
+    if dtype == "i32":
+        return v
+    return store(v.astype(np.float32), dtype)
+
+
+def worked(p: int = 2, n: int = 4096):
+    """Uniform ints in [-8, 8] as fp32; ranks 0 and 1 start with the worked example."""
+    xs = [uniform_int(n, SEEDS["worked"], r, -8, 8, "f32") for r in range(p)]
+    m = min(4, n)
+    xs[0][:m] = np.asarray(WORKED_A[:m], dtype=np.float32)
+    if p > 1:
+        xs[1][:m] = np.asarray(WORKED_B[:m], dtype=np.float32)
+    return xs
+
+
+def sweep(n: int, p: int = 8, dtype: str = "bf16"):
+    return [normal(n, SEEDS["sweep"], r, 1.0, dtype) for r in range(p)]
+
+
+def tp(tokens: int, p: int = 8, hidden: int = TP_HIDDEN, dtype: str = "bf16"):
+    return [normal(tokens * hidden, SEEDS["tp"], r, 0.02, dtype) for r in range(p)]
+
+
+def coverage(op: str, dtype: str, n: int = COVERAGE_N, p: int = 8):
+    s = SEEDS["coverage"]
+    if dtype == "i32":
+        if op == "prod":
+            return [choice(n, s, r, [-1, 1, 2], "i32") for r in range(p)]
+        return [uniform_int(n, s, r, -1000, 1000, "i32") for r in range(p)]
+    return [normal(n, s, r, 1.0, dtype) for r in range(p)]
+
+
+def moe(p: int = 16, shape=MOE_SHAPE, dtype: str = "bf16"):
+    n = shape[0] * shape[1]
+    return [normal(n, SEEDS["moe"], r, 1.0, dtype) for r in range(p)]
