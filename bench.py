@@ -1,0 +1,516 @@
+#!/usr/bin/env python3
+"""Benchmark: p=8 bf16 AllReduce throughput on one GPU, against HBM peak.
+
+One step = one ccl_allreduce call through the C ABI (argument checks,
+schedule selection and table build on the host, one fused kernel on the
+device) over p=8 rank buffers of 2^27 bf16 elements (256 MiB per rank,
+2 GiB in, 2 GiB out).  Throughput counts the algorithmic minimum bytes of an
+AllReduce in which every rank receives the result: p*n*s read + p*n*s written.
+
+Printed JSON line (rank 0): value = whole-job GB/s over K timed steps (CUDA
+events on the launching stream, barrier + synchronize on both sides, max over
+ranks), plus roofline (the fused kernel against the measured HBM copy peak),
+e2e (same metric with host buffers: pinned H2D copy, AllReduce, D2H copy
+inside the timed region), the CPU oracle baseline, clocks sampled during the
+timed region, and the message-size sweep (1 KiB .. 256 MiB per rank, ring and
+all-pairs).
+
+Multi-GPU: one process per GPU (torchrun), each an independent replica of the
+workload (the collective's p ranks are buffers in one GPU's memory; there is
+no exchange between GPUs).  value = all replicas' bytes / max time.
+
+--impl reference times the CPU oracle on the host cores instead (rank 0
+only), each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "p=8 bf16 AllReduce GB/s and % of GB300 HBM peak vs message size (1 GPU)"
+P = 8
+N = 1 << 27            # bf16 elements per rank: 256 MiB
+S = 2
+WORKLOAD = "p=8 bf16 AllReduce sum, 256 MiB per rank (n=2^27), N(0,1), schedule auto (ring at this size)"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["reducescatter_reduction_gb300/csrc/reduce.cuh",
+                  "reducescatter_reduction_gb300/csrc/device.cuh",
+                  "reducescatter_reduction_gb300/csrc/reduce_bf16.cu"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "allreduce_ldst_p8_bf16_256MiB.md")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--schedule", default="auto", choices=["auto", "ring", "allpairs"])
+    ap.add_argument("--variant", default="ldst", choices=["ldst", "tma", "tma_bulkred"])
+    ap.add_argument("--sm-budget", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# multi-process plumbing (timing only: no data moves between GPUs)
+# ---------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = False
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = True
+
+    def barrier(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def reduce(self, value: float, op: str) -> float:
+        """max or sum of a float over ranks (every rank gets the result)."""
+        if not self.pg:
+            return value
+        import torch
+        import torch.distributed as dist
+        dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([value], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+def aggregate(dist: Dist, local_ms: float, local_bytes: float):
+    """Whole-job throughput: every replica's bytes over the slowest replica's time."""
+    t = dist.reduce(local_ms, "max")
+    b = dist.reduce(local_bytes, "sum")
+    return t, b, (b / (t * 1e-3) / 1e9 if t > 0 else 0.0)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.gpu_id:
+                cmd.insert(1, f"--id={self.gpu_id}")
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = [line.strip().split(",") for line in self.file.read().splitlines() if line.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in rows:
+            row = [c.strip() for c in row]
+            if len(row) < 8:
+                continue
+            try:
+                sm.append(float(row[0]))
+                mx.append(float(row[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, row[4:8]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_uuid(torch, dev) -> str | None:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# peaks and the committed ncu summary
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: bf16 copy, read+write bytes)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            text = f.read()
+    except OSError:
+        return None
+    src, traffic = None, None
+    for line in text.splitlines():
+        if line.startswith("kernel_source_sha256_16:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    if src != kernel_source_hash():
+        return None
+    return traffic
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+
+def run_ours(args, dist: Dist):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import reducescatter_reduction_gb300 as ccl
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    dist.init("nccl")
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 0
+
+    # inputs: seeded N(0,1) bf16 on the device (2 GiB), outputs beside them
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2 + 1000 * dist.rank)
+    ins = [torch.randn(N, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+           for _ in range(P)]
+    outs = [torch.empty_like(t) for t in ins]
+    comm = ccl.ccl_comm_create(P, [t.data_ptr() for t in ins])
+    ccl.ccl_comm_set_outputs(comm, [t.data_ptr() for t in outs])
+    ccl.ccl_set_launch(comm, args.sm_budget, args.variant, 0)
+    alg_bytes = 2.0 * P * N * S
+
+    for _ in range(args.warmup):
+        ccl.ccl_allreduce(comm, "sum", "bf16", N, args.schedule, sptr)
+    torch.cuda.synchronize()
+    launch_desc = ccl.ccl_comm_last_launch(comm)
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_uuid(torch, dev))
+    sampler.start()
+    time.sleep(0.3)                       # let the sampler take its first reading
+    dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = ccl.ccl_comm_launch_count(comm)
+    e0.record(stream)
+    for _ in range(args.steps):
+        ccl.ccl_allreduce(comm, "sum", "bf16", N, args.schedule, sptr)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    launches = ccl.ccl_comm_launch_count(comm) - launches0
+    local_ms = e0.elapsed_time(e1)
+    ccl.ccl_comm_check(comm)
+
+    t_ms, job_bytes, job_gbs = aggregate(dist, local_ms, alg_bytes * args.steps)
+    ms_per_step = t_ms / args.steps
+    per_launch_ms = local_ms / max(1, launches)
+    achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+
+    result = {
+        "metric": METRIC,
+        "value": round(job_gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": dist.world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "frac_of_hbm_peak": round(job_gbs / dist.world / peak, 4),
+        "config": {
+            "workload": WORKLOAD,
+            "p": P, "n_per_rank": N, "element": "bf16 (fp32 accumulation)",
+            "bytes_per_rank": N * S,
+            "algorithmic_bytes_per_step": int(alg_bytes),
+            "schedule": args.schedule, "variant": args.variant, "sm_budget": args.sm_budget,
+            "launch": launch_desc,
+            "l2": f"inputs ({P * N * S >> 20} MiB) larger than L2 ({l2 >> 20} MiB): no flush",
+            "parallelism": f"replicas x{dist.world} (no inter-GPU exchange)",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(),
+            "algorithmic_bytes_per_launch": int(alg_bytes),
+            "peak_source": peak_src,
+            "kernel": launch_desc.split()[0] if launch_desc else None,
+        },
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes)
+
+    ccl.ccl_comm_destroy(comm)
+    if not args.no_sweep:
+        del outs
+        torch.cuda.empty_cache()
+        result["sweep"] = run_sweep(dist, dev, sptr, stream, peak, l2, ins)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline_from(ins)
+    del ins
+    dist.close()
+    return result
+
+
+def run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes):
+    """Same metric with host buffers: every step copies the p inputs from
+    pinned host memory, runs the AllReduce and copies the p results back."""
+    import torch
+    import reducescatter_reduction_gb300 as ccl
+
+    h_in = [torch.empty(N, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
+    h_out = [torch.empty(N, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
+    for h, d in zip(h_in, ins):
+        h.copy_(d)
+
+    def step():
+        for h, d in zip(h_in, ins):
+            d.copy_(h, non_blocking=True)
+        ccl.ccl_allreduce(comm, "sum", "bf16", N, args.schedule, sptr)
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t_ms, _, gbs = aggregate(dist, e0.elapsed_time(e1), alg_bytes * args.e2e_steps)
+    return {"value": round(gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": P * N * S,
+            "d2h_bytes_per_step": P * N * S, "steps": args.e2e_steps,
+            "ms_per_step": round(t_ms / args.e2e_steps, 4)}
+
+
+def run_sweep(dist, dev, sptr, stream, peak, l2, big_inputs):
+    """GB/s vs message size, 1 KiB .. 256 MiB per rank, ring and all-pairs.
+    Buffer sets rotate so that every timed call works on data that the
+    previous calls did not leave in L2 (>= 4 x L2 across the sets)."""
+    import torch
+    import reducescatter_reduction_gb300 as ccl
+
+    rows = []
+    l2 = l2 or (126 << 20)
+    for k in range(9, 28):
+        n = 1 << k
+        per_set = 2 * P * n * S
+        sets = 1 if per_set >= 4 * l2 else min(64, max(3, math.ceil(4 * l2 / per_set)))
+        comms, keep = [], []
+        for i in range(sets):
+            if n == N and i == 0:
+                src = big_inputs
+            else:
+                src = [torch.randn(n, device=dev, dtype=torch.float32).to(torch.bfloat16) for _ in range(P)]
+            dst = [torch.empty_like(t) for t in src]
+            h = ccl.ccl_comm_create(P, [t.data_ptr() for t in src])
+            ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in dst])
+            comms.append(h)
+            keep.append((src, dst))
+        row = {"bytes_per_rank": n * S, "rotating_sets": sets}
+        for sched in ("ring", "allpairs"):
+            iters = max(20, min(2000, int(0.2 / max(per_set / 5e12, 5e-6))))
+            for i in range(10):
+                ccl.ccl_allreduce(comms[i % sets], "sum", "bf16", n, sched, sptr)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(iters):
+                ccl.ccl_allreduce(comms[i % sets], "sum", "bf16", n, sched, sptr)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / iters
+            gbs = per_set / (us * 1e-6) / 1e9
+            row[sched] = {"us": round(us, 3), "GBps": round(gbs, 1),
+                          "frac_of_hbm_peak": round(gbs / peak, 4) if per_set >= 4 * l2 else None}
+        rows.append(row)
+        for h in comms:
+            ccl.ccl_comm_destroy(h)
+        del keep
+        torch.cuda.empty_cache()
+    return rows
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (the baseline; also the --impl reference arm)
+# ---------------------------------------------------------------------------
+
+def _time_oracle(xs, reps=1):
+    import oracle
+    t = time.perf_counter()
+    for _ in range(reps):
+        oracle.allreduce(xs, "sum", "bf16", "ring")
+    return (time.perf_counter() - t) / reps
+
+
+def cpu_baseline_from(ins):
+    """Time the oracle, as it stands (single-threaded C), on a slice of the
+    benchmark's own inputs sized to ~10-15 s of CPU work."""
+    import numpy as np
+    import torch
+
+    def host_slice(n):
+        return [t[:n].view(torch.int16).cpu().numpy().view(np.uint16).copy() for t in ins]
+
+    probe_n = 1 << 20
+    rate = probe_n / _time_oracle(host_slice(probe_n))   # elements per second per call
+    n = probe_n
+    while n * 2 <= N and (n * 2) / rate <= 15.0:
+        n *= 2
+    secs = _time_oracle(host_slice(n))
+    gbs = 2.0 * P * n * S / secs / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} elements (2^{int(math.log2(n))}) of each of the 8 rank buffers of the "
+                      f"benchmark workload, one single-threaded ring AllReduce call, {secs:.2f} s",
+            "seconds": round(secs, 3)}
+
+
+def run_reference(args, dist: Dist):
+    """The CPU oracle, timed on the host cores, on bounded samples of the
+    workload: each step one oracle AllReduce of n_s elements per rank."""
+    import numpy as np
+    from reducescatter_reduction_gb300 import inputs
+
+    if dist.rank != 0:
+        return None
+    probe = 1 << 18
+    xs = inputs.sweep(probe, P)
+    rate = probe / _time_oracle(xs, reps=3)
+    budget = 90.0 / max(1, args.steps + args.warmup)      # whole run within ~1.5 min
+    n = probe
+    while n * 2 <= N and (n * 2) / rate <= budget:
+        n *= 2
+    while n > 512 and n / rate > budget:
+        n //= 2
+    xs = inputs.sweep(n, P)
+    for _ in range(args.warmup):
+        _time_oracle(xs)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _time_oracle(xs)
+    secs = time.perf_counter() - t
+    gbs = 2.0 * P * n * S * args.steps / secs / 1e9
+    sample = (f"p=8 bf16 ring AllReduce of n={n} (2^{int(math.log2(n))}) elements per rank per step, "
+              "a slice of the 2^27-element workload; single-threaded C oracle")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(gbs, 4),
+        "unit": "GB/s",
+        "n_gpus": dist.world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample, "p": P, "n_per_step": n},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dist = Dist()
+    if args.impl == "reference":
+        res = run_reference(args, dist)
+    else:
+        res = run_ours(args, dist)
+    if dist.rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,254 @@
+/*
+ * ccl.h -- AllReduce, ReduceScatter and AllGather over p "rank" buffers that
+ * all live in the memory of one GPU (NVIDIA GB300, sm_103a).
+ *
+ * What is computed.  "Inside NCCL AllReduce", section "What all-reduce
+ * promises": all-reduce takes one same-shaped buffer per rank, combines them
+ * element-wise with sum, prod, min, max or avg, and leaves every rank holding
+ * the identical result; it equals a reduce-scatter (each rank ends owning the
+ * finished reduction of one slice) followed by an all-gather (the finished
+ * slices go to every rank).  Here the p ranks are p device buffers; there
+ * are no peer GPUs and no messages.  Each element is reduced once, in fp32
+ * for floating-point types (int32 for int32), in the exact rank order that
+ * the schedule gives its chunk, and the finished value is written to every
+ * destination in the same pass.
+ *
+ * Schedules (chunk c is elements [c*q + min(c, r), ...) with q = n / p,
+ * r = n % p, i.e. p balanced chunks, larger ones first):
+ *  - CCL_SCHED_RING: "Inside NCCL AllReduce", section "The ring, exactly as
+ *    the kernel runs it" -- a chunk gathers one more rank's contribution per
+ *    hop and completes at its owner.  Chunk c is accumulated in rank order
+ *    (c+1) mod p, (c+2) mod p, ..., c (the three-GPU state table: chunk a
+ *    starts as a1, adds a2, is completed by a0 on GPU 0).
+ *  - CCL_SCHED_ALLPAIRS: "MSCCL, in depth", section "Writing an algorithm in
+ *    MSCCLang" -- every rank sends slice r to owner r, which reduces it and
+ *    broadcasts it; slice r is accumulated in rank order 0, 1, ..., p-1.
+ *  - CCL_SCHED_CUSTOM: the per-chunk orders set by ccl_comm_set_schedule().
+ *  - CCL_SCHED_AUTO: the alpha-beta cost model of "MSCCL, in depth" (sections
+ *    "Why generic collectives leave time on the table" and "Worked example:
+ *    all-pairs versus ring on 8 GPUs") picks ring or all-pairs; see
+ *    ccl_select_schedule().  The environment variable CCL_SCHEDULE=ring|allpairs
+ *    overrides AUTO only.
+ *
+ * Numerics.  fp16/bf16/fp32 inputs are widened exactly to fp32; partial
+ * results stay fp32 for all p-1 steps; the result is rounded once to the
+ * element type, round-to-nearest-even.  sum: fp32 add (no fused multiply-add);
+ * prod: fp32 multiply; min/max: acc = (v < acc) ? v : acc (resp. >), so the
+ * earlier operand in the schedule order wins ties; avg: each floating-point
+ * contribution is multiplied by fl32(1/p) as it is read, and an int32 avg is
+ * the wrapped int32 sum divided by p with truncation toward zero ("Inside
+ * NCCL AllReduce", "What all-reduce promises").  int32 sum/prod wrap modulo
+ * 2^32.  The ld/st and TMA copy variants keep this order exactly; the TMA
+ * bulk-reduce variant (CCL_VARIANT_TMA_BULKRED) lets the memory system apply
+ * the adds and is held to |err| <= 2 * p * eps(element type) * sum_k |x_k|
+ * per element instead.
+ *
+ * Memory and ownership.  The caller allocates and owns every rank buffer
+ * (device memory, e.g. from PyTorch).  A communicator copies the p input and
+ * output pointers (host arrays are not retained) and allocates one small
+ * device status block (256 bytes) that it frees in ccl_comm_destroy().  No
+ * call allocates memory proportional to the message.
+ *
+ * Asynchrony.  The collective calls check their arguments on the host,
+ * enqueue kernels on `stream` (a cudaStream_t passed as void*, NULL = the
+ * legacy default stream) and return without synchronising.  Errors detected
+ * on the host are returned at once; a bounded device-side wait that gave up
+ * is reported by ccl_comm_check().
+ *
+ * Alignment.  All pointers 16-byte aligned (and, for ReduceScatter /
+ * AllGather, (n/p) * element size a multiple of 16) take the 128-bit vector
+ * path; other layouts take a correct element-wise path (no error).
+ *
+ * Threads.  A communicator must not be used from two host threads at once.
+ * ccl_last_error() is per host thread.
+ */
+#ifndef CCL_H
+#define CCL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CCL_API __attribute__((visibility("default")))
+#else
+#define CCL_API
+#endif
+
+#define CCL_MAX_RANKS 64
+#define CCL_VERSION 10000 /* 1.0.0 */
+
+typedef struct ccl_comm *ccl_comm_t;
+
+typedef enum {
+    CCL_OK = 0,
+    CCL_ERR_INVALID_ARG = 1, /* bad pointer, size, alias, enum value, schedule table */
+    CCL_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (e.g. bulk-reduce of prod) */
+    CCL_ERR_CUDA = 3,        /* a CUDA runtime call failed; ccl_last_error() names it */
+    CCL_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (see ccl_comm_check) */
+    CCL_ERR_NOMEM = 5        /* host or device allocation failed */
+} ccl_status_t;
+
+typedef enum { CCL_SUM = 0, CCL_PROD = 1, CCL_MIN = 2, CCL_MAX = 3, CCL_AVG = 4 } ccl_op_t;
+
+typedef enum { CCL_F32 = 0, CCL_F16 = 1, CCL_BF16 = 2, CCL_I32 = 3 } ccl_dtype_t;
+
+typedef enum {
+    CCL_SCHED_AUTO = 0,
+    CCL_SCHED_RING = 1,
+    CCL_SCHED_ALLPAIRS = 2,
+    CCL_SCHED_CUSTOM = 3
+} ccl_schedule_t;
+
+typedef enum {
+    CCL_VARIANT_AUTO = 0,    /* ld/st unless an SM budget below the whole GPU favours TMA */
+    CCL_VARIANT_LDST = 1,    /* 128-bit register loads/stores, fixed order */
+    CCL_VARIANT_TMA = 2,     /* cp.async.bulk into shared-memory stages, fixed order */
+    CCL_VARIANT_TMA_BULKRED = 3 /* cp.reduce.async.bulk: order left to the memory system */
+} ccl_variant_t;
+
+/* ---------------------------------------------------------------------------
+ * Communicator.
+ * ------------------------------------------------------------------------- */
+
+/* Create a communicator over p rank buffers.
+ *  out        : receives the handle (host pointer, must not be NULL).
+ *  p          : number of ranks, 1 <= p <= CCL_MAX_RANKS.
+ *  rank_ptrs  : host array of p device pointers; rank_ptrs[r] is rank r's
+ *               input buffer.  Copied; the array may be freed on return.
+ *               Outputs default to the inputs (in place).
+ * The current CUDA device at creation is the device every call runs on.
+ * T-CCL, section "Programming Model": each rank passes its local buffer
+ * and the communication group resolves the peers.
+ * Errors: CCL_ERR_INVALID_ARG (NULL out/rank_ptrs, a NULL buffer, p out of
+ * range), CCL_ERR_CUDA, CCL_ERR_NOMEM. */
+CCL_API ccl_status_t ccl_comm_create(ccl_comm_t *out, int p, void *const *rank_ptrs);
+
+/* Set the p output buffers (host array of device pointers, copied).  NULL
+ * restores in-place operation (outputs = inputs).  Aliasing is checked at
+ * each call, since only then are sizes known. */
+CCL_API ccl_status_t ccl_comm_set_outputs(ccl_comm_t comm, void *const *out_ptrs);
+
+/* Set the per-chunk accumulation orders used by CCL_SCHED_CUSTOM.
+ * order: host array of p*p bytes; order[c*p + k] is the k-th rank folded
+ * into chunk c.  Rejected (CCL_ERR_INVALID_ARG) unless every row is a
+ * permutation of 0..p-1 -- the validation of "MSCCL, in depth" (Check():
+ * the program computes the declared collective). */
+CCL_API ccl_status_t ccl_comm_set_schedule(ccl_comm_t comm, const uint8_t *order);
+
+/* Launch shape.
+ *  sm_budget : 0 = all SMs; k > 0 = at most k CTAs, one per SM (persistent),
+ *              the restricted-CTA-budget setting of T-CCL, section
+ *              "Collective Operation Performance" (Fig. 4, Table IV).  Larger than the SM count = all SMs.
+ *  variant   : a ccl_variant_t.
+ *  pipeline_chunk_bytes : 0 = the variant's default.  For the TMA variants,
+ *              the bytes per rank moved per pipeline stage (multiple of 16,
+ *              1 KiB .. 32 KiB).  Results never depend on it.
+ * Errors: CCL_ERR_INVALID_ARG for a negative budget, an unknown variant or a
+ * chunk size outside the range. */
+CCL_API ccl_status_t ccl_set_launch(ccl_comm_t comm, int sm_budget, int variant,
+                            size_t pipeline_chunk_bytes);
+
+/* Release the communicator and its device status block.  Waits for
+ * nothing: the caller must not destroy a communicator whose kernels are
+ * still in flight.  NULL is accepted. */
+CCL_API ccl_status_t ccl_comm_destroy(ccl_comm_t comm);
+
+/* Synchronise the communicator's device and read its status block.
+ * CCL_ERR_TIMEOUT if a bounded wait in a kernel gave up since the last
+ * check (the block is then cleared), CCL_ERR_CUDA on a CUDA error,
+ * otherwise CCL_OK. */
+CCL_API ccl_status_t ccl_comm_check(ccl_comm_t comm);
+
+/* ---------------------------------------------------------------------------
+ * Collectives.  n is always the element count of one full rank buffer.
+ * ------------------------------------------------------------------------- */
+
+/* AllReduce: out[r][e] = reduction over ranks of in[k][e], for every r and
+ * every e < n, each chunk in its schedule order.  In place (out[r] ==
+ * in[r]) or out of place; any other overlap between an output and any
+ * buffer is CCL_ERR_INVALID_ARG.  Any n >= 0 (n == 0 is a no-op).
+ * Bytes moved: p*n*s read + p*n*s written. */
+CCL_API ccl_status_t ccl_allreduce(ccl_comm_t comm, ccl_op_t op, ccl_dtype_t dtype, size_t n,
+                           ccl_schedule_t schedule, void *stream);
+
+/* ReduceScatter: out[r][i] = element c_r + i of the reduction, 0 <= i < n/p,
+ * where c_r = r*n/p: rank r receives its own chunk, written from offset 0.
+ * Requires n % p == 0 (else CCL_ERR_INVALID_ARG, never a silent fallback).
+ * In place in NCCL's sense (out[r] == in[r] + r*n/p elements) or disjoint.
+ * Bytes moved: p*n*s read + n*s written. */
+CCL_API ccl_status_t ccl_reduce_scatter(ccl_comm_t comm, ccl_op_t op, ccl_dtype_t dtype, size_t n,
+                                ccl_schedule_t schedule, void *stream);
+
+/* AllGather: rank r contributes elements [r*n/p, (r+1)*n/p) of its input
+ * buffer in[r] (n elements); every rank's output out[k] receives all n
+ * elements, rank r's chunk at offset r*n/p.  Requires n % p == 0.  In place
+ * (out[k] == in[k]: the owner's own chunk is not rewritten) or disjoint.
+ * Bytes moved: n*s read + p*n*s written (in place: (p-1)*n*s written). */
+CCL_API ccl_status_t ccl_all_gather(ccl_comm_t comm, ccl_dtype_t dtype, size_t n, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Host-side schedule builder and cost model (no GPU needed).
+ * ------------------------------------------------------------------------- */
+
+/* Build the per-chunk table of a schedule.
+ *  bounds : host array of p+1 entries; chunk c is [bounds[c], bounds[c+1]).
+ *  order  : host array of p*p bytes; order[c*p + k] = k-th rank folded into c.
+ * schedule must be CCL_SCHED_RING or CCL_SCHED_ALLPAIRS.
+ * The owner of chunk c (ReduceScatter destination) is rank c. */
+CCL_API ccl_status_t ccl_schedule_build(int p, uint64_t n, ccl_schedule_t schedule,
+                                uint64_t *bounds, uint8_t *order);
+
+/* Validate a table: bounds partition [0, n) in order, every row of order is
+ * a permutation of 0..p-1.  CCL_OK or CCL_ERR_INVALID_ARG. */
+CCL_API ccl_status_t ccl_schedule_check(int p, uint64_t n, const uint64_t *bounds,
+                                const uint8_t *order);
+
+/* Alpha-beta model parameters ("MSCCL, in depth"): alpha_s per synchronised
+ * step, link bandwidth in bytes/s, and the protocol efficiency each schedule
+ * runs at (LL = 0.5, LL128 = 120/128 on the page). */
+typedef struct {
+    double alpha_s;
+    double bw_bytes_per_s;
+    double eff_ring;
+    double eff_allpairs;
+} ccl_cost_params_t;
+
+/* Modelled time (seconds) of AllReduce of nbytes per rank over p ranks:
+ * ring 2(p-1)*alpha + 2(p-1)/p * nbytes / (bw*eff_ring); all-pairs
+ * 2*alpha + 2(p-1)/p * nbytes / (bw*eff_allpairs).  params NULL = the
+ * page's worked-example values (2 us, 300 GB/s, 120/128, 0.5).
+ * Returns a negative value for bad arguments. */
+CCL_API double ccl_cost_estimate(int p, double nbytes, ccl_schedule_t schedule,
+                         const ccl_cost_params_t *params);
+
+/* The schedule AUTO resolves to: the lower modelled time (ties: ring). */
+CCL_API ccl_schedule_t ccl_select_schedule(int p, double nbytes, const ccl_cost_params_t *params);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics.
+ * ------------------------------------------------------------------------- */
+
+/* Message for the last non-OK status returned on this host thread. */
+CCL_API const char *ccl_last_error(void);
+
+/* Description of the last kernel launch this communicator issued (kernel,
+ * dtype, op, p, n, schedule, variant, grid, block, shared memory), so that
+ * a caller can prove which path ran.  Copies at most len-1 characters plus
+ * a terminating NUL into buf; returns CCL_ERR_INVALID_ARG if buf is NULL. */
+CCL_API ccl_status_t ccl_comm_last_launch(ccl_comm_t comm, char *buf, size_t len);
+
+/* Number of kernels this communicator has launched since creation. */
+CCL_API uint64_t ccl_comm_launch_count(ccl_comm_t comm);
+
+/* CCL_VERSION of the loaded library. */
+CCL_API int ccl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCL_H */

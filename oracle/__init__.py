@@ -58,6 +58,7 @@ def lib():
         L.oracle_allreduce.argtypes = [i32, u64, i32, i32, i32, pp, pp]
         L.oracle_reduce_scatter.argtypes = [i32, u64, i32, i32, i32, pp, pp]
         L.oracle_all_gather.argtypes = [i32, u64, i32, pp, pp]
+        L.oracle_allreduce_orders.argtypes = [i32, u64, i32, i32, ctypes.POINTER(ctypes.c_uint8), pp, pp]
         L.oracle_allreduce_at.argtypes = [i32, u64, i32, i32, i32, pp,
                                           ctypes.POINTER(u64), u64, vp]
         L.oracle_chunk_bounds.argtypes = [i32, u64, i32, ctypes.POINTER(u64), ctypes.POINTER(u64)]
@@ -104,6 +105,22 @@ def allreduce(xs, op, dtype, schedule="ring"):
     rc = lib().oracle_allreduce(len(xs), n, dt, o, s, _ptrs(xs), _ptrs(ys))
     if rc:
         raise ValueError("oracle_allreduce rejected its arguments")
+    return ys
+
+
+def allreduce_orders(xs, op, dtype, order):
+    """AllReduce with explicit per-chunk orders: order[c][k] is the k-th rank
+    folded into chunk c."""
+    dt, o = _code(DTYPES, dtype), _code(OPS, op)
+    _check_inputs(xs, dt)
+    p, n = len(xs), xs[0].size
+    flat = [int(v) for row in order for v in row]
+    if len(flat) != p * p:
+        raise ValueError("order must be p rows of p ranks")
+    arr = (ctypes.c_uint8 * (p * p))(*flat)
+    ys = [np.empty(n, dtype=NP_STORAGE[dt]) for _ in xs]
+    if lib().oracle_allreduce_orders(p, n, dt, o, arr, _ptrs(xs), _ptrs(ys)):
+        raise ValueError("oracle_allreduce_orders rejected its arguments")
     return ys
 
 

@@ -212,25 +212,46 @@ static int check_args(int p, int dtype, int op, int schedule)
 /* Collectives.                                                             */
 /* ------------------------------------------------------------------------ */
 
+/* AllReduce with explicit per-chunk orders: order[c*p + k] is the k-th rank
+ * folded into chunk c (each row a permutation of 0..p-1).  Every rank's
+ * output y[k] receives all n elements. */
+int oracle_allreduce_orders(int p, uint64_t n, int dtype, int op, const uint8_t *order,
+                            const void *const *x, void *const *y)
+{
+    if (check_args(p, dtype, op, OR_RING)) return -1;
+    size_t s = (dtype == OR_F32 || dtype == OR_I32) ? 4 : 2;
+    int ord[64];
+    for (int c = 0; c < p; ++c) {
+        uint64_t seen = 0;
+        for (int k = 0; k < p; ++k) {
+            ord[k] = order[c * p + k];
+            if (ord[k] >= p || ((seen >> ord[k]) & 1u)) return -1;
+            seen |= (uint64_t)1 << ord[k];
+        }
+        uint64_t b, en;
+        oracle_chunk_bounds(p, n, c, &b, &en);
+        for (uint64_t e = b; e < en; ++e) {
+            reduce_element(p, dtype, op, ord, x, e, y[0], e);
+            for (int k = 1; k < p; ++k)             /* the finished chunk goes to every rank */
+                memcpy((char *)y[k] + e * s, (const char *)y[0] + e * s, s);
+        }
+    }
+    return 0;
+}
+
 /* AllReduce: every rank's output y[k] receives the full reduction, all n
  * elements; chunk c is reduced in its schedule order. */
 int oracle_allreduce(int p, uint64_t n, int dtype, int op, int schedule,
                      const void *const *x, void *const *y)
 {
     if (check_args(p, dtype, op, schedule)) return -1;
-    size_t s = (dtype == OR_F32 || dtype == OR_I32) ? 4 : 2;
-    int order[64];
+    uint8_t order[64 * 64];
+    int row[64];
     for (int c = 0; c < p; ++c) {
-        uint64_t b, en;
-        oracle_chunk_bounds(p, n, c, &b, &en);
-        oracle_chunk_order(p, schedule, c, order);
-        for (uint64_t e = b; e < en; ++e) {
-            reduce_element(p, dtype, op, order, x, e, y[0], e);
-            for (int k = 1; k < p; ++k)             /* the finished chunk goes to every rank */
-                memcpy((char *)y[k] + e * s, (const char *)y[0] + e * s, s);
-        }
+        oracle_chunk_order(p, schedule, c, row);
+        for (int k = 0; k < p; ++k) order[c * p + k] = (uint8_t)row[k];
     }
-    return 0;
+    return oracle_allreduce_orders(p, n, dtype, op, order, x, y);
 }
 
 /* ReduceScatter: rank r's output y[r] receives chunk r of the reduction,

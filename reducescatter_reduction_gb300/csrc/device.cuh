@@ -1,0 +1,215 @@
+// Device-side helpers: 128-bit global loads/stores with cache hints, and the
+// per-element-type arithmetic of the reduction (widen to fp32, fold in order,
+// round once to the element type).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "internal.h"
+
+namespace ccl {
+
+// ---------------------------------------------------------------------------
+// Memory access.  Inputs are streamed once: read through the non-coherent
+// path without allocating in L1, with a 256-byte L2 prefetch hint.  Each
+// element is read and then written by the same thread and by no other, so an
+// in-place operation never reads a value another thread has written.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_v4(void *p, const uint4 &v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Element types.  Each traits class gives: the accumulator type, VEC =
+// elements per 16 bytes, unpacking a 16-byte vector into VEC accumulator
+// values, packing VEC finished values back, and single-element load/store.
+// ---------------------------------------------------------------------------
+
+struct F32 {};
+struct F16 {};
+struct BF16 {};
+struct I32 {};
+
+template <typename T> struct Traits;
+
+template <> struct Traits<F32> {
+    using Acc = float;
+    static constexpr int VEC = 4;
+    static constexpr int kDtype = DT_F32;
+    __device__ static void unpack(const uint4 &v, float (&f)[VEC])
+    {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ static uint4 pack(const float (&f)[VEC])
+    {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+    __device__ static float load1(const void *base, uint64_t e)
+    {
+        return static_cast<const float *>(base)[e];
+    }
+    __device__ static void store1(void *base, uint64_t e, float v)
+    {
+        static_cast<float *>(base)[e] = v;
+    }
+};
+
+// bf16 is the upper half of an fp32 word: widening is a 16-bit shift.
+template <> struct Traits<BF16> {
+    using Acc = float;
+    static constexpr int VEC = 8;
+    static constexpr int kDtype = DT_BF16;
+    __device__ static void unpack(const uint4 &v, float (&f)[VEC])
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ static uint32_t pack2(float lo, float hi)
+    {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ static uint4 pack(const float (&f)[VEC])
+    {
+        return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
+                          pack2(f[6], f[7]));
+    }
+    __device__ static float load1(const void *base, uint64_t e)
+    {
+        return __uint_as_float(uint32_t(static_cast<const uint16_t *>(base)[e]) << 16);
+    }
+    __device__ static void store1(void *base, uint64_t e, float v)
+    {
+        __nv_bfloat16 h = __float2bfloat16_rn(v);
+        static_cast<uint16_t *>(base)[e] = *reinterpret_cast<uint16_t *>(&h);
+    }
+};
+
+template <> struct Traits<F16> {
+    using Acc = float;
+    static constexpr int VEC = 8;
+    static constexpr int kDtype = DT_F16;
+    __device__ static void unpack(const uint4 &v, float (&f)[VEC])
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+            float2 t = __half22float2(h);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+    __device__ static uint32_t pack2(float lo, float hi)
+    {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ static uint4 pack(const float (&f)[VEC])
+    {
+        return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
+                          pack2(f[6], f[7]));
+    }
+    __device__ static float load1(const void *base, uint64_t e)
+    {
+        return __half2float(static_cast<const __half *>(base)[e]);
+    }
+    __device__ static void store1(void *base, uint64_t e, float v)
+    {
+        static_cast<__half *>(base)[e] = __float2half_rn(v);
+    }
+};
+
+// int32 accumulates in uint32 so that sum and prod wrap modulo 2^32.
+template <> struct Traits<I32> {
+    using Acc = uint32_t;
+    static constexpr int VEC = 4;
+    static constexpr int kDtype = DT_I32;
+    __device__ static void unpack(const uint4 &v, uint32_t (&f)[VEC])
+    {
+        f[0] = v.x;
+        f[1] = v.y;
+        f[2] = v.z;
+        f[3] = v.w;
+    }
+    __device__ static uint4 pack(const uint32_t (&f)[VEC]) { return make_uint4(f[0], f[1], f[2], f[3]); }
+    __device__ static uint32_t load1(const void *base, uint64_t e)
+    {
+        return static_cast<const uint32_t *>(base)[e];
+    }
+    __device__ static void store1(void *base, uint64_t e, uint32_t v)
+    {
+        static_cast<uint32_t *>(base)[e] = v;
+    }
+};
+
+// ---------------------------------------------------------------------------
+// The fold.  `first` turns the first contribution into the accumulator,
+// `fold` adds one more (acc = acc (+) v), `finish` produces the stored value.
+// Floating point: explicit round-to-nearest intrinsics, so no multiply-add
+// is ever contracted; min/max by compare-and-select (earlier operand wins
+// ties, exactly as written, not fminf/fmaxf).
+// ---------------------------------------------------------------------------
+
+template <int OP> struct FoldF {
+    __device__ static __forceinline__ float first(float v, float scale)
+    {
+        return OP == OP_AVG ? __fmul_rn(v, scale) : v;
+    }
+    __device__ static __forceinline__ float fold(float acc, float v, float scale)
+    {
+        if constexpr (OP == OP_SUM) return __fadd_rn(acc, v);
+        else if constexpr (OP == OP_AVG) return __fadd_rn(acc, __fmul_rn(v, scale));
+        else if constexpr (OP == OP_PROD) return __fmul_rn(acc, v);
+        else if constexpr (OP == OP_MIN) return (v < acc) ? v : acc;
+        else return (v > acc) ? v : acc;
+    }
+    __device__ static __forceinline__ float finish(float acc, int) { return acc; }
+};
+
+template <int OP> struct FoldI {
+    __device__ static __forceinline__ uint32_t first(uint32_t v, float) { return v; }
+    __device__ static __forceinline__ uint32_t fold(uint32_t acc, uint32_t v, float)
+    {
+        if constexpr (OP == OP_SUM || OP == OP_AVG) return acc + v;
+        else if constexpr (OP == OP_PROD) return acc * v;
+        else if constexpr (OP == OP_MIN) return (int32_t(v) < int32_t(acc)) ? v : acc;
+        else return (int32_t(v) > int32_t(acc)) ? v : acc;
+    }
+    // int avg: the wrapped sum divided once by p, truncating toward zero
+    __device__ static __forceinline__ uint32_t finish(uint32_t acc, int p)
+    {
+        if constexpr (OP == OP_AVG) return uint32_t(int32_t(acc) / p);
+        else return acc;
+    }
+};
+
+template <typename T, int OP>
+using Fold = typename std::conditional<std::is_same<T, I32>::value, FoldI<OP>, FoldF<OP>>::type;
+
+}  // namespace ccl

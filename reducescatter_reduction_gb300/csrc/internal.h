@@ -1,0 +1,67 @@
+// Internal interface between the host front end (ccl.cpp) and the kernel
+// translation units.  Not installed; the public interface is include/ccl.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ccl {
+
+constexpr int kMaxRanks = 64;
+
+enum Op : int { OP_SUM = 0, OP_PROD = 1, OP_MIN = 2, OP_MAX = 3, OP_AVG = 4 };
+enum Dtype : int { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_I32 = 3 };
+enum Mode : int { MODE_AR = 0, MODE_RS = 1 };
+
+inline size_t elem_bytes(int dtype) { return (dtype == DT_F16 || dtype == DT_BF16) ? 2 : 4; }
+
+// One chunk table: chunk c is elements [bound[c], bound[c+1]) and is folded
+// in rank order order[c*p + 0], order[c*p + 1], ...
+struct Table {
+    int p = 0;
+    uint64_t n = 0;
+    uint64_t bound[kMaxRanks + 1];
+    uint8_t order[kMaxRanks * kMaxRanks];
+};
+
+// What the front end decided; the kernel TUs turn it into a launch.
+struct Launch {
+    int p = 0;
+    int op = 0;
+    int dtype = 0;
+    int mode = MODE_AR;
+    uint64_t n = 0;
+    const void *src[kMaxRanks];
+    void *dst[kMaxRanks];
+    const Table *table = nullptr;
+    bool vec = false;          // 16-byte vector body allowed
+    uint64_t self_mask = 0;    // AllGather: bit r set when dst[r] == src[r] (in place)
+    int num_sms = 0;
+    int sm_budget = 0;         // 0 = all SMs
+    size_t pipe_bytes = 0;     // TMA stage bytes per rank
+    unsigned *status = nullptr;  // device status block
+    long long wait_limit_ns = 0;
+    int stall_test = 0;
+    cudaStream_t stream = nullptr;
+};
+
+// Filled by a launcher for diagnostics.
+struct LaunchInfo {
+    const char *kernel = "";
+    int grid = 0;
+    int block = 0;
+    size_t smem = 0;
+    int kernels = 0;           // kernels launched
+};
+
+// Per-dtype AllReduce / ReduceScatter launchers (ld/st variant).
+cudaError_t launch_reduce_f32(const Launch &L, LaunchInfo *info);
+cudaError_t launch_reduce_f16(const Launch &L, LaunchInfo *info);
+cudaError_t launch_reduce_bf16(const Launch &L, LaunchInfo *info);
+cudaError_t launch_reduce_i32(const Launch &L, LaunchInfo *info);
+
+// AllGather (broadcast store), dtype-agnostic beyond the element size.
+cudaError_t launch_gather(const Launch &L, LaunchInfo *info);
+
+}  // namespace ccl

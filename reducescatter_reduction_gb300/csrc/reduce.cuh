@@ -1,0 +1,252 @@
+// Multi-source reduce: the core of ReduceScatter and, fused with the
+// broadcast store, of AllReduce.
+//
+// "Inside NCCL AllReduce", section "The ring, exactly as the kernel runs it":
+// the ring all-reduce is one fused loop whose workhorse step receives a
+// partial sum, adds the local contribution in registers and forwards it,
+// never storing partials in between.  With all p ranks in one GPU's memory
+// the p-1 hops of a chunk collapse into one thread: it loads the p
+// contributions of a 16-byte group (one 128-bit load per rank), folds them in
+// fp32 in exactly the chunk's rank order, rounds once, and stores the result
+// to every rank (AllReduce) or to the chunk's owner (ReduceScatter).  Bytes
+// moved are the minimum: p*n*s read, p*n*s (AR) or n*s (RS) written.
+//
+// Work split: the buffer is a flat sequence of 16-byte groups handed out
+// grid-stride (all CTAs sweep the rank buffers together, so each rank's
+// stream stays DRAM-page local).  A group lying wholly in one chunk takes the
+// vector path; a group straddling a chunk boundary (only when a chunk size is
+// not a multiple of the group) and the sub-group tail are done element by
+// element with each element's own chunk order.
+#pragma once
+
+#include "device.cuh"
+
+namespace ccl {
+
+constexpr int kReduceThreads = 256;
+
+template <int PM>
+struct ReduceArgs {
+    const void *src[PM];        // rank inputs
+    void *dst[PM];              // rank outputs (RS: dst[c] receives chunk c from offset 0)
+    uint64_t bound[PM + 1];     // chunk c = elements [bound[c], bound[c+1])
+    uint8_t order[PM][PM];      // order[c][k]: k-th rank folded into chunk c
+    uint64_t n;                 // elements per rank
+    int p;
+    int vec;                    // 1: 16-byte groups allowed (all pointers aligned)
+    float scale;                // avg: fl32(1/p)
+};
+
+// One element e of chunk c, folded in the chunk's order.
+template <typename T, int OP, int MODE, int PM>
+__device__ __forceinline__ void reduce_one(const ReduceArgs<PM> &a, int p, int c, uint64_t e)
+{
+    using Tr = Traits<T>;
+    using F = Fold<T, OP>;
+    auto acc = F::first(Tr::load1(a.src[a.order[c][0]], e), a.scale);
+    for (int k = 1; k < p; ++k)
+        acc = F::fold(acc, Tr::load1(a.src[a.order[c][k]], e), a.scale);
+    const auto out = F::finish(acc, p);
+    if constexpr (MODE == MODE_AR) {
+        for (int k = 0; k < p; ++k) Tr::store1(a.dst[k], e, out);
+    } else {
+        Tr::store1(a.dst[c], e - a.bound[c], out);
+    }
+}
+
+// P > 0: p fixed at compile time (loads fully unrolled); P == 0: any p up to
+// kMaxRanks, loads issued eight at a time.
+template <typename T, int OP, int P, int MODE>
+__global__ void __launch_bounds__(kReduceThreads)
+    reduce_kernel(const __grid_constant__ ReduceArgs<(P > 0 ? P : kMaxRanks)> a)
+{
+    using Tr = Traits<T>;
+    using F = Fold<T, OP>;
+    using Acc = typename Tr::Acc;
+    constexpr int VEC = Tr::VEC;
+    constexpr int ES = int(sizeof(Acc));     // element bytes of the 4-byte types
+    constexpr int S = (VEC == 8) ? 2 : ES;   // element bytes
+    const int p = P > 0 ? P : a.p;
+
+    const uint64_t tid = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+    const uint64_t ngroups = a.vec ? a.n / VEC : 0;
+
+    int c = 0;
+    uint64_t cend = a.bound[1];
+    const char *sp[P > 0 ? P : 1];  // P > 0: chunk c's sources, already in fold order
+    if constexpr (P > 0) {
+#pragma unroll
+        for (int k = 0; k < P; ++k) sp[k] = static_cast<const char *>(a.src[a.order[0][k]]);
+    }
+
+    for (uint64_t g = tid; g < ngroups; g += stride) {
+        const uint64_t e = g * VEC;
+        if (e >= cend) {  // next chunk(s); empty chunks are skipped
+            do { ++c; } while (e >= a.bound[c + 1]);
+            cend = a.bound[c + 1];
+            if constexpr (P > 0) {
+#pragma unroll
+                for (int k = 0; k < P; ++k) sp[k] = static_cast<const char *>(a.src[a.order[c][k]]);
+            }
+        }
+        if (e + VEC > cend) {  // straddles a chunk boundary: per element
+            int cj = c;
+            for (int j = 0; j < VEC; ++j) {
+                while (e + j >= a.bound[cj + 1]) ++cj;
+                reduce_one<T, OP, MODE>(a, p, cj, e + j);
+            }
+            continue;
+        }
+        Acc acc[VEC];
+        if constexpr (P > 0) {
+            uint4 r[P];
+#pragma unroll
+            for (int k = 0; k < P; ++k) r[k] = ld_stream_v4(sp[k] + e * S);
+            Acc v[VEC];
+            Tr::unpack(r[0], v);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) acc[i] = F::first(v[i], a.scale);
+#pragma unroll
+            for (int k = 1; k < P; ++k) {
+                Tr::unpack(r[k], v);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) acc[i] = F::fold(acc[i], v[i], a.scale);
+            }
+        } else {
+            for (int k0 = 0; k0 < p; k0 += 8) {
+                uint4 r[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (k0 + j < p)
+                        r[j] = ld_stream_v4(static_cast<const char *>(a.src[a.order[c][k0 + j]]) + e * S);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (k0 + j < p) {
+                        Acc v[VEC];
+                        Tr::unpack(r[j], v);
+                        if (k0 + j == 0) {
+#pragma unroll
+                            for (int i = 0; i < VEC; ++i) acc[i] = F::first(v[i], a.scale);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < VEC; ++i) acc[i] = F::fold(acc[i], v[i], a.scale);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) acc[i] = F::finish(acc[i], p);
+        const uint4 out = Tr::pack(acc);
+        if constexpr (MODE == MODE_AR) {
+            if constexpr (P > 0) {
+#pragma unroll
+                for (int k = 0; k < P; ++k) st_v4(static_cast<char *>(a.dst[k]) + e * S, out);
+            } else {
+                for (int k = 0; k < p; ++k) st_v4(static_cast<char *>(a.dst[k]) + e * S, out);
+            }
+        } else {
+            st_v4(static_cast<char *>(a.dst[c]) + (e - a.bound[c]) * S, out);
+        }
+    }
+
+    // Elements after the last whole group (every element when vec == 0).
+    int ct = 0;
+    for (uint64_t e = ngroups * VEC + tid; e < a.n; e += stride) {
+        while (e >= a.bound[ct + 1]) ++ct;
+        reduce_one<T, OP, MODE>(a, p, ct, e);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: pick the instantiation, fill the argument block, size the grid.
+// ---------------------------------------------------------------------------
+
+template <typename T, int OP, int P, int MODE>
+static cudaError_t launch_p(const Launch &L, LaunchInfo *info)
+{
+    constexpr int PM = P > 0 ? P : kMaxRanks;
+    ReduceArgs<PM> a;
+    for (int k = 0; k < L.p; ++k) {
+        a.src[k] = L.src[k];
+        a.dst[k] = L.dst[k];
+    }
+    for (int c = 0; c <= L.p; ++c) a.bound[c] = L.table->bound[c];
+    for (int c = 0; c < L.p; ++c)
+        for (int k = 0; k < L.p; ++k) a.order[c][k] = L.table->order[c * L.p + k];
+    a.n = L.n;
+    a.p = L.p;
+    a.vec = L.vec ? 1 : 0;
+    a.scale = 1.0f / float(L.p);
+
+    auto kern = reduce_kernel<T, OP, P, MODE>;
+    static int occ = -1;  // resident CTAs per SM for this instantiation
+    if (occ < 0) {
+        int b = 0;
+        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kReduceThreads, 0);
+        if (err != cudaSuccess) return err;
+        occ = b > 0 ? b : 1;
+    }
+    const uint64_t units = L.vec ? (L.n / Traits<T>::VEC + L.n % Traits<T>::VEC) : L.n;
+    uint64_t want = (units + kReduceThreads - 1) / kReduceThreads;
+    if (want < 1) want = 1;
+    uint64_t cap = uint64_t(L.num_sms) * occ;
+    if (L.sm_budget > 0 && uint64_t(L.sm_budget) < uint64_t(L.num_sms)) cap = uint64_t(L.sm_budget);
+    const int grid = int(want < cap ? want : cap);
+    // A budgeted launch must not put two CTAs on one SM: ask for more than
+    // half of an SM's shared memory so that at most one fits.
+    size_t smem = 0;
+    if (L.sm_budget > 0 && L.sm_budget < L.num_sms) {
+        smem = 120 * 1024;
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+            if (err != cudaSuccess) return err;
+            attr = true;
+        }
+    }
+    kern<<<grid, kReduceThreads, smem, L.stream>>>(a);
+    if (info) {
+        info->kernel = MODE == MODE_AR ? "allreduce_ldst" : "reduce_scatter_ldst";
+        info->grid = grid;
+        info->block = kReduceThreads;
+        info->smem = smem;
+        info->kernels = 1;
+    }
+    return cudaGetLastError();
+}
+
+template <typename T, int OP, int MODE>
+static cudaError_t launch_op_mode(const Launch &L, LaunchInfo *info)
+{
+    switch (L.p) {
+    case 2: return launch_p<T, OP, 2, MODE>(L, info);
+    case 4: return launch_p<T, OP, 4, MODE>(L, info);
+    case 8: return launch_p<T, OP, 8, MODE>(L, info);
+    case 16: return launch_p<T, OP, 16, MODE>(L, info);
+    default: return launch_p<T, OP, 0, MODE>(L, info);
+    }
+}
+
+template <typename T, int OP>
+static cudaError_t launch_op(const Launch &L, LaunchInfo *info)
+{
+    return L.mode == MODE_AR ? launch_op_mode<T, OP, MODE_AR>(L, info)
+                             : launch_op_mode<T, OP, MODE_RS>(L, info);
+}
+
+template <typename T>
+static cudaError_t launch_reduce(const Launch &L, LaunchInfo *info)
+{
+    switch (L.op) {
+    case OP_SUM: return launch_op<T, OP_SUM>(L, info);
+    case OP_PROD: return launch_op<T, OP_PROD>(L, info);
+    case OP_MIN: return launch_op<T, OP_MIN>(L, info);
+    case OP_MAX: return launch_op<T, OP_MAX>(L, info);
+    case OP_AVG: return launch_op<T, OP_AVG>(L, info);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace ccl

@@ -139,6 +139,37 @@ def test_order_pin_first_rank(fixture, p, sched, op, dtype):
             assert neg == (expected[c][0] == j), (c, j)
 
 
+@pytest.mark.parametrize("p", [3, 5, 8])
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_order_pin_custom_tables(p, dtype):
+    """The explicit-order entry folds each chunk in exactly the order given:
+    random permutation tables, observed through the same absorption probe."""
+    rng = np.random.default_rng(p)
+    table = [list(rng.permutation(p)) for _ in range(p)]
+    triples, n, xs = _triple_probe(p, dtype)
+    T = len(triples)
+    y = as_float(oracle.allreduce_orders(xs, "sum", dtype, table)[0], dtype)
+    for c in range(p):
+        got = y[c * T:(c + 1) * T] != 0
+        want = np.array([_survives(table[c], *t) for t in triples])
+        assert np.array_equal(got, want), f"chunk {c}"
+    # first position, through the signed-zero probe
+    vals = np.zeros((p, p * p), dtype=np.float32)
+    for c in range(p):
+        for j in range(p):
+            vals[j, c * p + j] = -0.0
+    y = as_float(oracle.allreduce_orders([to_storage(v, dtype) for v in vals], "min", dtype, table)[0], dtype)
+    for c in range(p):
+        for j in range(p):
+            assert (math.copysign(1.0, y[c * p + j]) < 0) == (table[c][0] == j)
+
+
+def test_custom_orders_reject_non_permutations():
+    xs = [np.zeros(6, dtype=np.float32)] * 3
+    with pytest.raises(ValueError):
+        oracle.allreduce_orders(xs, "sum", "f32", [[0, 1, 2], [1, 1, 2], [2, 0, 1]])
+
+
 def test_chunk_order_listing_matches_fixtures():
     for fixture, p, sched in [("ring_order_p3.txt", 3, "ring"), ("ring_order_p4.txt", 4, "ring"),
                               ("ring_order_p8.txt", 8, "ring"),

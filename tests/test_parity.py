@@ -1,0 +1,426 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle
+on the same seeded inputs.  Fixed-order results must be bit-identical
+(every op, every dtype, both schedules).  Full-size workloads compare sampled
+elements one by one with the oracle and check size-independent properties
+(all ranks identical, schedule invariance of exact ops, invariance to the
+launch shape)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import reducescatter_reduction_gb300 as ccl
+from reducescatter_reduction_gb300 import inputs
+from ccl_testutil import (Comm, RankBuffers, bits_equal, ensure_built, sample_indices,
+                          stream_ptr)
+from conftest import read_golden
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["f32", "f16", "bf16", "i32"]
+OPS = ["sum", "prod", "min", "max", "avg"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    ensure_built()
+
+
+def gen(dtype, op, p, n, seed):
+    """Seeded rank buffers for an op: small ints for prod (exact, no overflow
+    to inf), uniform ints for int32, normals otherwise."""
+    if dtype == "i32":
+        if op == "prod":
+            return [inputs.choice(n, seed, r, [-1, 1, 2], "i32") for r in range(p)]
+        return [inputs.uniform_int(n, seed, r, -1000, 1000, "i32") for r in range(p)]
+    if op == "prod":
+        return [inputs.choice(n, seed, r, [-2, -1, 1, 2], dtype) for r in range(p)]
+    return [inputs.normal(n, seed, r, 1.0, dtype) for r in range(p)]
+
+
+def run_collective(xs, coll, op, dtype, sched="ring", inplace=False, offset=0, budget=0,
+                   variant="ldst", n=None):
+    storage = inputs.STORAGE[dtype]
+    p = len(xs)
+    n = xs[0].size if n is None else n
+    ins = RankBuffers(xs, n, storage, offset=offset)
+    out_n = n // p if coll == "rs" else n
+    outs = None if inplace else RankBuffers(None, out_n, storage, p=p, offset=offset)
+    with Comm(ins, outs) as cm:
+        ccl.ccl_set_launch(cm.h, budget, variant, 0)
+        before = ccl.ccl_comm_launch_count(cm.h)
+        if coll == "ar":
+            ccl.ccl_allreduce(cm.h, op, dtype, n, sched, stream_ptr())
+        elif coll == "rs":
+            ccl.ccl_reduce_scatter(cm.h, op, dtype, n, sched, stream_ptr())
+        else:
+            ccl.ccl_all_gather(cm.h, dtype, n, stream_ptr())
+        torch.cuda.synchronize()
+        launched = ccl.ccl_comm_launch_count(cm.h) - before
+        desc = ccl.ccl_comm_last_launch(cm.h)
+    res = ins if inplace else outs
+    assert ins.guards_intact(), "write outside the buffers"
+    if outs is not None:
+        assert outs.guards_intact(), "write outside the output buffers"
+    if n:
+        assert launched >= 1, "no kernel ran"
+    return res, desc
+
+
+# ---------------------------------------------------------------------------
+# the worked example workload
+# ---------------------------------------------------------------------------
+
+def test_worked_example_workload():
+    rows = {r[0]: [float(v) for v in r[1:]] for r in read_golden("worked_example.txt")}
+    xs = inputs.worked()
+    res, desc = run_collective(xs, "ar", "sum", "f32", "ring")
+    want = oracle.allreduce(xs, "sum", "f32", "ring")
+    for r in range(2):
+        got = res.host(r)
+        assert got[:4].tolist() == rows["result"]
+        assert bits_equal(got, want[r])
+    assert "allreduce_ldst" in desc and "schedule=ring" in desc and "vec=1" in desc
+
+
+# ---------------------------------------------------------------------------
+# small shapes: every op x dtype x schedule, many p and n (incl. empty and
+# sizes that are not multiples of the 16-byte group or of p)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("sched", ["ring", "allpairs"])
+def test_allreduce_small_exhaustive(dtype, op, sched):
+    for p in (1, 2, 3, 8, 16, 17, 64):
+        for n in (0, 1, 9, 65, 1027):
+            xs = gen(dtype, op, p, n, seed=1000 + p)
+            res, _ = run_collective(xs, "ar", op, dtype, sched)
+            want = oracle.allreduce(xs, op, dtype, sched)
+            for r in range(p):
+                assert bits_equal(res.host(r), want[r]), (p, n, r)
+
+
+# ---------------------------------------------------------------------------
+# several grid sweeps, ragged tails, chunk boundaries off the 16-byte grid
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("p,dtype,op,sched", [
+    (8, "bf16", "sum", "ring"), (8, "bf16", "avg", "allpairs"), (16, "bf16", "sum", "ring"),
+    (5, "f32", "sum", "ring"), (4, "f16", "max", "ring"), (8, "i32", "prod", "allpairs"),
+    (3, "f32", "min", "allpairs"), (2, "bf16", "prod", "ring"), (24, "f16", "avg", "ring"),
+    (16, "i32", "avg", "ring"),
+])
+def test_allreduce_multi_sweep_ragged(p, dtype, op, sched):
+    n = 3 * (1 << 20) + 13
+    xs = gen(dtype, op, p, n, seed=7)
+    res, desc = run_collective(xs, "ar", op, dtype, sched)
+    want = oracle.allreduce(xs, op, dtype, sched)
+    for r in range(p):
+        assert bits_equal(res.host(r), want[r]), r
+    assert "vec=1" in desc
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_allreduce_in_place(dtype):
+    p, n = 8, (1 << 18) + 5
+    xs = gen(dtype, "sum", p, n, seed=8)
+    res, _ = run_collective(xs, "ar", "sum", dtype, "ring", inplace=True)
+    want = oracle.allreduce(xs, "sum", dtype, "ring")
+    for r in range(p):
+        assert bits_equal(res.host(r), want[r])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("coll", ["ar", "rs", "ag"])
+def test_misaligned_pointers_take_elementwise_path(dtype, coll):
+    p, n = 4, 4 * 1000
+    s = inputs.ELEM_BYTES[dtype]
+    xs = gen(dtype, "sum", p, n, seed=9)
+    res, desc = run_collective(xs, coll, "sum", dtype, "allpairs", offset=s)
+    assert "vec=0" in desc
+    if coll == "ar":
+        want = oracle.allreduce(xs, "sum", dtype, "allpairs")
+    elif coll == "rs":
+        want = oracle.reduce_scatter(xs, "sum", dtype, "allpairs")
+    else:
+        want = oracle.all_gather(xs, dtype)
+    for r in range(p):
+        assert bits_equal(res.host(r), want[r])
+
+
+# ---------------------------------------------------------------------------
+# ReduceScatter and AllGather
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("op", OPS)
+def test_reduce_scatter(dtype, op):
+    for p, n, sched in ((2, 2 * 4099, "ring"), (3, 3 * 1000, "allpairs"), (8, 8 * 65536, "ring"),
+                        (16, 16 * 513, "allpairs"), (1, 77, "ring")):
+        xs = gen(dtype, op, p, n, seed=11)
+        res, _ = run_collective(xs, "rs", op, dtype, sched)
+        want = oracle.reduce_scatter(xs, op, dtype, sched)
+        for r in range(p):
+            assert bits_equal(res.host(r), want[r]), (p, r)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_reduce_scatter_in_place_nccl_convention(dtype):
+    """In place as NCCL defines it: rank r's output is chunk r of its own
+    input buffer."""
+    p, n = 8, 8 * 40000
+    xs = gen(dtype, "sum", p, n, seed=12)
+    storage = inputs.STORAGE[dtype]
+    ins = RankBuffers(xs, n, storage)
+    with Comm(ins, out_ptrs=[ins.ptr(r, r * (n // p)) for r in range(p)]) as cm:
+        ccl.ccl_reduce_scatter(cm.h, "sum", dtype, n, "ring", stream_ptr())
+        torch.cuda.synchronize()
+    want = oracle.reduce_scatter(xs, "sum", dtype, "ring")
+    for r in range(p):
+        got = ins.host(r)[r * (n // p):(r + 1) * (n // p)]
+        assert bits_equal(got, want[r])
+    assert ins.guards_intact()
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("inplace", [False, True])
+def test_all_gather(dtype, inplace):
+    for p, n in ((2, 2 * 4099), (3, 3 * 1000), (8, 8 * 65536), (16, 16 * 513), (5, 5 * 8)):
+        xs = gen(dtype, "sum", p, n, seed=13)
+        res, _ = run_collective(xs, "ag", None, dtype, inplace=inplace)
+        want = oracle.all_gather(xs, dtype)
+        for r in range(p):
+            assert bits_equal(res.host(r), want[r]), (p, r)
+
+
+@pytest.mark.parametrize("tokens", inputs.TP_TOKENS)
+def test_tp_activation_allreduce_equals_rs_then_ag(tokens):
+    """Tensor-parallel activations [tokens, 8192] at TP=8: AllReduce matches
+    the oracle, and ReduceScatter (rank r gets [tokens, 1024]) followed by an
+    in-place AllGather gives the same bits ("Inside NCCL AllReduce": all-reduce
+    = reduce-scatter + all-gather)."""
+    p, dtype = 8, "bf16"
+    xs = inputs.tp(tokens, p)
+    n = xs[0].size
+    storage = inputs.STORAGE[dtype]
+    ar, _ = run_collective(xs, "ar", "sum", dtype, "ring")
+    if n <= 256 * 8192:
+        want = oracle.allreduce(xs, "sum", dtype, "ring")
+        for r in range(p):
+            assert bits_equal(ar.host(r), want[r])
+    else:
+        idx = sample_indices(p, n)
+        want = oracle.allreduce_at(xs, idx, "sum", dtype, "ring")
+        for r in range(p):
+            assert bits_equal(ar.at(r, idx), want)
+    ins = RankBuffers(xs, n, storage)
+    z = RankBuffers(None, n, storage, p=p)
+    chunk = n // p
+    with Comm(ins, out_ptrs=[z.ptr(r, r * chunk) for r in range(p)]) as cm:
+        ccl.ccl_reduce_scatter(cm.h, "sum", dtype, n, "ring", stream_ptr())
+    with Comm(z) as cm:                        # in place: out[r] == in[r]
+        ccl.ccl_all_gather(cm.h, dtype, n, stream_ptr())
+    torch.cuda.synchronize()
+    for r in range(p):
+        assert torch.equal(z.views[r], ar.views[r]), r
+    assert z.guards_intact()
+
+
+# ---------------------------------------------------------------------------
+# custom schedules
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("p", [3, 8, 16, 20])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_custom_schedule(p, dtype):
+    rng = np.random.default_rng(p)
+    table = [list(rng.permutation(p)) for _ in range(p)]
+    n = p * 10007 + 3
+    xs = gen(dtype, "sum", p, n, seed=14)
+    storage = inputs.STORAGE[dtype]
+    ins = RankBuffers(xs, n, storage)
+    outs = RankBuffers(None, n, storage, p=p)
+    with Comm(ins, outs) as cm:
+        ccl.ccl_comm_set_schedule(cm.h, table)
+        ccl.ccl_allreduce(cm.h, "sum", dtype, n, "custom", stream_ptr())
+        torch.cuda.synchronize()
+        assert "schedule=custom" in ccl.ccl_comm_last_launch(cm.h)
+    want = oracle.allreduce_orders(xs, "sum", dtype, table)
+    for r in range(p):
+        assert bits_equal(outs.host(r), want[r])
+
+
+# ---------------------------------------------------------------------------
+# schedule selection, launch accounting, streams
+# ---------------------------------------------------------------------------
+
+def test_auto_schedule_follows_cost_model(monkeypatch):
+    p = 8
+    for n, want in ((1 << 10, "allpairs"), (1 << 24, "ring")):
+        xs = gen("bf16", "sum", p, n, seed=15)
+        _, desc = run_collective(xs, "ar", "sum", "bf16", "auto")
+        assert f"schedule={want}" in desc
+        assert ccl.ccl_select_schedule(p, n * 2) == (ccl.CCL_SCHED_ALLPAIRS if want == "allpairs"
+                                                     else ccl.CCL_SCHED_RING)
+    monkeypatch.setenv("CCL_SCHEDULE", "ring")
+    xs = gen("bf16", "sum", p, 1 << 10, seed=15)
+    _, desc = run_collective(xs, "ar", "sum", "bf16", "auto")
+    assert "schedule=ring" in desc
+
+
+def test_side_stream_and_launch_count():
+    p, n, dtype = 8, 1 << 20, "bf16"
+    xs = gen(dtype, "sum", p, n, seed=16)
+    storage = inputs.STORAGE[dtype]
+    ins = RankBuffers(xs, n, storage)
+    outs = RankBuffers(None, n, storage, p=p)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with Comm(ins, outs) as cm:
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                ccl.ccl_allreduce(cm.h, "sum", dtype, n, "ring", side.cuda_stream)
+        side.synchronize()
+        assert ccl.ccl_comm_launch_count(cm.h) == 3
+    want = oracle.allreduce(xs, "sum", dtype, "ring")
+    assert bits_equal(outs.host(5), want[5])
+
+
+# ---------------------------------------------------------------------------
+# errors: explicit statuses, never a silent fallback
+# ---------------------------------------------------------------------------
+
+def test_argument_errors():
+    p, n = 4, 4 * 256
+    xs = gen("f32", "sum", p, n, seed=17)
+    ins = RankBuffers(xs, n, np.float32)
+    outs = RankBuffers(None, n, np.float32, p=p)
+    with Comm(ins, outs) as cm:
+        def status(fn, *a):
+            try:
+                fn(*a)
+                return ccl.CCL_OK
+            except ccl.CclError as e:
+                return e.status
+        s = stream_ptr()
+        assert status(ccl.ccl_reduce_scatter, cm.h, "sum", "f32", n + 1, "ring", s) == ccl.CCL_ERR_INVALID_ARG
+        assert status(ccl.ccl_all_gather, cm.h, "f32", n - 2, s) == ccl.CCL_ERR_INVALID_ARG
+        assert status(ccl.ccl_allreduce, cm.h, 9, "f32", n, "ring", s) == ccl.CCL_ERR_INVALID_ARG
+        assert status(ccl.ccl_allreduce, cm.h, "sum", 7, n, "ring", s) == ccl.CCL_ERR_INVALID_ARG
+        assert status(ccl.ccl_allreduce, cm.h, "sum", "f32", n, 9, s) == ccl.CCL_ERR_INVALID_ARG
+        assert status(ccl.ccl_allreduce, cm.h, "sum", "f32", n, "custom", s) == ccl.CCL_ERR_INVALID_ARG
+        assert status(ccl.ccl_comm_set_schedule, cm.h, [[0, 1, 2, 2]] * 4) == ccl.CCL_ERR_INVALID_ARG
+        assert status(ccl.ccl_set_launch, cm.h, -1, "ldst", 0) == ccl.CCL_ERR_INVALID_ARG
+        assert status(ccl.ccl_set_launch, cm.h, 0, 9, 0) == ccl.CCL_ERR_INVALID_ARG
+        assert status(ccl.ccl_set_launch, cm.h, 0, "tma", 100) == ccl.CCL_ERR_INVALID_ARG
+        # overlapping outputs
+        ccl.ccl_comm_set_outputs(cm.h, [outs.ptr(0), outs.ptr(0, 10), outs.ptr(2), outs.ptr(3)])
+        assert status(ccl.ccl_allreduce, cm.h, "sum", "f32", n, "ring", s) == ccl.CCL_ERR_INVALID_ARG
+        # an output overlapping another rank's input
+        ccl.ccl_comm_set_outputs(cm.h, [ins.ptr(1), outs.ptr(1), outs.ptr(2), outs.ptr(3)])
+        assert status(ccl.ccl_allreduce, cm.h, "sum", "f32", n, "ring", s) == ccl.CCL_ERR_INVALID_ARG
+        # ReduceScatter written at offset 0 of its own (n-element) input overlaps chunk 0
+        ccl.ccl_comm_set_outputs(cm.h, [ins.ptr(r) for r in range(p)])
+        assert status(ccl.ccl_reduce_scatter, cm.h, "sum", "f32", n, "ring", s) == ccl.CCL_ERR_INVALID_ARG
+        # n == 0 is a no-op
+        ccl.ccl_comm_set_outputs(cm.h, None)
+        count = ccl.ccl_comm_launch_count(cm.h)
+        ccl.ccl_allreduce(cm.h, "sum", "f32", 0, "ring", s)
+        assert ccl.ccl_comm_launch_count(cm.h) == count
+        ccl.ccl_comm_check(cm.h)
+    torch.cuda.synchronize()
+    assert ins.guards_intact() and outs.guards_intact()
+    for r in range(p):                         # nothing was written
+        assert bits_equal(ins.host(r), xs[r])
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads
+# ---------------------------------------------------------------------------
+
+def test_sweep_bf16_p8():
+    """p=8 bf16 N(0,1), 1 KiB .. 256 MiB per rank, ring and all-pairs, in the
+    launch shape the benchmark times (all SMs, ld/st): full comparison up to
+    512 KiB per rank, sampled beyond; all ranks identical."""
+    p = 8
+    for n in inputs.SWEEP_N:
+        xs = inputs.sweep(n, p)
+        for sched in ("ring", "allpairs"):
+            res, desc = run_collective(xs, "ar", "sum", "bf16", sched)
+            assert "vec=1" in desc and f"schedule={sched}" in desc
+            if n <= 1 << 18:
+                want = oracle.allreduce(xs, "sum", "bf16", sched)
+                for r in range(p):
+                    assert bits_equal(res.host(r), want[r]), (n, sched)
+            else:
+                idx = sample_indices(p, n, count=50000, seed=n)
+                want = oracle.allreduce_at(xs, idx, "sum", "bf16", sched)
+                assert bits_equal(res.at(0, idx), want), (n, sched)
+                assert bits_equal(res.at(p - 1, idx), want), (n, sched)
+                assert res.identical_across_ranks(), (n, sched)
+            del res
+        del xs
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("dtype,ops", [("i32", ["sum", "min", "max", "prod"]),
+                                       ("f32", ["avg", "sum", "max"]),
+                                       ("f16", ["avg", "sum", "max"])])
+def test_op_coverage_64M(dtype, ops):
+    """p=8, n = 64 Mi per rank: int32 results bit-exact and identical under
+    both schedules; fp32/fp16 avg (1/p folded into the kernel), sum, max."""
+    p, n = 8, inputs.COVERAGE_N
+    idx = sample_indices(p, n, count=50000, seed=4)
+    cache = {}
+    for op in ops:
+        key = op == "prod"
+        if key not in cache:
+            cache.clear()
+            cache[key] = inputs.coverage(op, dtype, n=n, p=p)
+        xs = cache[key]
+        res, _ = run_collective(xs, "ar", op, dtype, "ring")
+        want = oracle.allreduce_at(xs, idx, op, dtype, "ring")
+        assert bits_equal(res.at(0, idx), want), op
+        assert res.identical_across_ranks(), op
+        if dtype == "i32" or op == "max":
+            res2, _ = run_collective(xs, "ar", op, dtype, "allpairs")
+            assert torch.equal(res.views[0], res2.views[0]), op
+            del res2
+        del res
+        torch.cuda.empty_cache()
+
+
+def test_moe_p16_sm_budgets():
+    """p=16 bf16 [16384, 7168] per rank (224 MiB each), ring: sampled oracle
+    comparison, and the same bits at SM budgets 4, 8, 16 and all."""
+    p, dtype = 16, "bf16"
+    xs = inputs.moe(p)
+    n = xs[0].size
+    idx = sample_indices(p, n, count=50000, seed=5)
+    want = oracle.allreduce_at(xs, idx, "sum", dtype, "ring")
+    storage = inputs.STORAGE[dtype]
+    ins = RankBuffers(xs, n, storage)
+    del xs
+    ref = None
+    for budget in (0, 4, 8, 16):
+        outs = RankBuffers(None, n, storage, p=p)
+        with Comm(ins, outs) as cm:
+            ccl.ccl_set_launch(cm.h, budget, "ldst", 0)
+            ccl.ccl_allreduce(cm.h, "sum", dtype, n, "ring", stream_ptr())
+            torch.cuda.synchronize()
+            desc = ccl.ccl_comm_last_launch(cm.h)
+        grid = int(desc.split("grid=")[1].split()[0])
+        if budget:
+            assert grid <= budget
+        assert bits_equal(outs.at(0, idx), want)
+        assert outs.identical_across_ranks()
+        if ref is None:
+            ref = outs.views[0].clone()
+        else:
+            assert torch.equal(outs.views[0], ref), budget
+        assert outs.guards_intact()
+        del outs
+        torch.cuda.empty_cache()
