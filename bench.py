@@ -64,6 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--n", type=int, default=N,
+                    help="bf16 elements per rank (default 2^27; smaller only for profiling runs)")
     return ap.parse_args(argv)
 
 
@@ -211,7 +213,10 @@ def profiled_traffic():
         if line.startswith("kernel_source_sha256_16:"):
             src = line.split(":", 1)[1].strip()
         if line.startswith("dram_bytes_per_launch:"):
-            traffic = float(line.split(":", 1)[1].strip())
+            try:
+                traffic = float(line.split(":", 1)[1].strip())
+            except ValueError:
+                traffic = None
     if src != kernel_source_hash():
         return None
     return traffic
@@ -240,16 +245,17 @@ def run_ours(args, dist: Dist):
     # inputs: seeded N(0,1) bf16 on the device (2 GiB), outputs beside them
     gen = torch.Generator(device=dev)
     gen.manual_seed(2 + 1000 * dist.rank)
-    ins = [torch.randn(N, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    n = args.n
+    ins = [torch.randn(n, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
            for _ in range(P)]
     outs = [torch.empty_like(t) for t in ins]
     comm = ccl.ccl_comm_create(P, [t.data_ptr() for t in ins])
     ccl.ccl_comm_set_outputs(comm, [t.data_ptr() for t in outs])
     ccl.ccl_set_launch(comm, args.sm_budget, args.variant, 0)
-    alg_bytes = 2.0 * P * N * S
+    alg_bytes = 2.0 * P * n * S
 
     for _ in range(args.warmup):
-        ccl.ccl_allreduce(comm, "sum", "bf16", N, args.schedule, sptr)
+        ccl.ccl_allreduce(comm, "sum", "bf16", n, args.schedule, sptr)
     torch.cuda.synchronize()
     launch_desc = ccl.ccl_comm_last_launch(comm)
 
@@ -263,7 +269,7 @@ def run_ours(args, dist: Dist):
     launches0 = ccl.ccl_comm_launch_count(comm)
     e0.record(stream)
     for _ in range(args.steps):
-        ccl.ccl_allreduce(comm, "sum", "bf16", N, args.schedule, sptr)
+        ccl.ccl_allreduce(comm, "sum", "bf16", n, args.schedule, sptr)
     e1.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
@@ -293,13 +299,13 @@ def run_ours(args, dist: Dist):
         "data": "synthetic",
         "frac_of_hbm_peak": round(job_gbs / dist.world / peak, 4),
         "config": {
-            "workload": WORKLOAD,
-            "p": P, "n_per_rank": N, "element": "bf16 (fp32 accumulation)",
-            "bytes_per_rank": N * S,
+            "workload": WORKLOAD if n == N else f"p=8 bf16 AllReduce sum, n={n} per rank (profiling size)",
+            "p": P, "n_per_rank": n, "element": "bf16 (fp32 accumulation)",
+            "bytes_per_rank": n * S,
             "algorithmic_bytes_per_step": int(alg_bytes),
             "schedule": args.schedule, "variant": args.variant, "sm_budget": args.sm_budget,
             "launch": launch_desc,
-            "l2": f"inputs ({P * N * S >> 20} MiB) larger than L2 ({l2 >> 20} MiB): no flush",
+            "l2": f"inputs ({P * n * S >> 20} MiB) larger than L2 ({l2 >> 20} MiB): no flush",
             "parallelism": f"replicas x{dist.world} (no inter-GPU exchange)",
         },
         "roofline": {
@@ -308,7 +314,7 @@ def run_ours(args, dist: Dist):
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(),
+            "traffic": profiled_traffic() if n == N else None,
             "algorithmic_bytes_per_launch": int(alg_bytes),
             "peak_source": peak_src,
             "kernel": launch_desc.split()[0] if launch_desc else None,
@@ -318,7 +324,7 @@ def run_ours(args, dist: Dist):
     }
 
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes)
+        result["e2e"] = run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes, n)
 
     ccl.ccl_comm_destroy(comm)
     if not args.no_sweep:
@@ -332,21 +338,21 @@ def run_ours(args, dist: Dist):
     return result
 
 
-def run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes):
+def run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes, n):
     """Same metric with host buffers: every step copies the p inputs from
     pinned host memory, runs the AllReduce and copies the p results back."""
     import torch
     import reducescatter_reduction_gb300 as ccl
 
-    h_in = [torch.empty(N, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
-    h_out = [torch.empty(N, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
+    h_in = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
+    h_out = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
     for h, d in zip(h_in, ins):
         h.copy_(d)
 
     def step():
         for h, d in zip(h_in, ins):
             d.copy_(h, non_blocking=True)
-        ccl.ccl_allreduce(comm, "sum", "bf16", N, args.schedule, sptr)
+        ccl.ccl_allreduce(comm, "sum", "bf16", n, args.schedule, sptr)
         for h, d in zip(h_out, outs):
             h.copy_(d, non_blocking=True)
 
@@ -364,8 +370,8 @@ def run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes):
     torch.cuda.synchronize()
     dist.barrier()
     t_ms, _, gbs = aggregate(dist, e0.elapsed_time(e1), alg_bytes * args.e2e_steps)
-    return {"value": round(gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": P * N * S,
-            "d2h_bytes_per_step": P * N * S, "steps": args.e2e_steps,
+    return {"value": round(gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": P * n * S,
+            "d2h_bytes_per_step": P * n * S, "steps": args.e2e_steps,
             "ms_per_step": round(t_ms / args.e2e_steps, 4)}
 
 
@@ -384,7 +390,7 @@ def run_sweep(dist, dev, sptr, stream, peak, l2, big_inputs):
         sets = 1 if per_set >= 4 * l2 else min(64, max(3, math.ceil(4 * l2 / per_set)))
         comms, keep = [], []
         for i in range(sets):
-            if n == N and i == 0:
+            if n == big_inputs[0].numel() and i == 0:
                 src = big_inputs
             else:
                 src = [torch.randn(n, device=dev, dtype=torch.float32).to(torch.bfloat16) for _ in range(P)]
@@ -442,7 +448,7 @@ def cpu_baseline_from(ins):
     probe_n = 1 << 20
     rate = probe_n / _time_oracle(host_slice(probe_n))   # elements per second per call
     n = probe_n
-    while n * 2 <= N and (n * 2) / rate <= 15.0:
+    while n * 2 <= ins[0].numel() and (n * 2) / rate <= 15.0:
         n *= 2
     secs = _time_oracle(host_slice(n))
     gbs = 2.0 * P * n * S / secs / 1e9
