@@ -325,6 +325,8 @@ def run_ours(args, dist: Dist):
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes, n)
+    if not args.no_sweep:
+        result["rs_ag"] = run_rs_ag(args, ins, outs, sptr, stream, peak, n)
 
     ccl.ccl_comm_destroy(comm)
     if not args.no_sweep:
@@ -373,6 +375,41 @@ def run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes, n):
     return {"value": round(gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": P * n * S,
             "d2h_bytes_per_step": P * n * S, "steps": args.e2e_steps,
             "ms_per_step": round(t_ms / args.e2e_steps, 4)}
+
+
+def run_rs_ag(args, ins, outs, sptr, stream, peak, n):
+    """The same buffers as separate ReduceScatter (out[r] = chunk r) and
+    AllGather (in place): GB/s over each one's algorithmic bytes."""
+    import torch
+    import reducescatter_reduction_gb300 as ccl
+
+    chunk = n // P
+    rows = {}
+    rs = ccl.ccl_comm_create(P, [t.data_ptr() for t in ins])
+    ccl.ccl_comm_set_outputs(rs, [outs[r].data_ptr() + r * chunk * S for r in range(P)])
+    ag = ccl.ccl_comm_create(P, [t.data_ptr() for t in outs])
+    cases = (("reduce_scatter", lambda: ccl.ccl_reduce_scatter(rs, "sum", "bf16", n, "ring", sptr),
+              (P + 1) * n * S, rs),
+             ("all_gather_in_place", lambda: ccl.ccl_all_gather(ag, "bf16", n, sptr), P * n * S, ag))
+    for name, call, nbytes, h in cases:
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        iters = 200
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / iters
+        gbs = nbytes / (us * 1e-6) / 1e9
+        rows[name] = {"us": round(us, 2), "GBps": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+                      "algorithmic_bytes": nbytes, "launch": ccl.ccl_comm_last_launch(h)}
+    ccl.ccl_comm_destroy(rs)
+    ccl.ccl_comm_destroy(ag)
+    return rows
 
 
 def run_sweep(dist, dev, sptr, stream, peak, l2, big_inputs):

@@ -152,6 +152,18 @@ CCL_API ccl_status_t ccl_comm_set_schedule(ccl_comm_t comm, const uint8_t *order
 CCL_API ccl_status_t ccl_set_launch(ccl_comm_t comm, int sm_budget, int variant,
                             size_t pipeline_chunk_bytes);
 
+/* Failure-detection hooks (tests).
+ *  wait_limit_ns : bound on any single wait inside a kernel that waits (the
+ *                  TMA variant's pipeline barriers); 0 restores the default
+ *                  of 2 s.  On expiry the kernel records the wait in the
+ *                  status block, stops, and ccl_comm_check() returns
+ *                  CCL_ERR_TIMEOUT.
+ *  stall_test    : 1 makes the TMA producer withhold its second tile, so that
+ *                  the consumers' bounded wait runs out: the timeout path is
+ *                  exercised without faulting or hanging the GPU.  0 = off.
+ * Errors: CCL_ERR_INVALID_ARG for negative values or stall_test > 1. */
+CCL_API ccl_status_t ccl_comm_set_debug(ccl_comm_t comm, long long wait_limit_ns, int stall_test);
+
 /* Release the communicator and its device status block.  Waits for
  * nothing: the caller must not destroy a communicator whose kernels are
  * still in flight.  NULL is accepted. */

@@ -39,7 +39,7 @@ STATUS_NAMES = {CCL_OK: "CCL_OK", CCL_ERR_INVALID_ARG: "CCL_ERR_INVALID_ARG",
 
 # Every symbol include/ccl.h declares.
 EXPORTS = (
-    "ccl_comm_create", "ccl_comm_set_outputs", "ccl_comm_set_schedule", "ccl_set_launch",
+    "ccl_comm_create", "ccl_comm_set_outputs", "ccl_comm_set_schedule", "ccl_set_launch", "ccl_comm_set_debug",
     "ccl_comm_destroy", "ccl_comm_check", "ccl_allreduce", "ccl_reduce_scatter", "ccl_all_gather",
     "ccl_schedule_build", "ccl_schedule_check", "ccl_cost_estimate", "ccl_select_schedule",
     "ccl_last_error", "ccl_comm_last_launch", "ccl_comm_launch_count", "ccl_version",
@@ -76,6 +76,7 @@ def load_library(path: str = LIB_PATH):
         "ccl_comm_set_outputs": (i, [vp, pvp]),
         "ccl_comm_set_schedule": (i, [vp, ctypes.POINTER(ctypes.c_uint8)]),
         "ccl_set_launch": (i, [vp, i, i, sz]),
+        "ccl_comm_set_debug": (i, [vp, ctypes.c_longlong, i]),
         "ccl_comm_destroy": (i, [vp]),
         "ccl_comm_check": (i, [vp]),
         "ccl_allreduce": (i, [vp, i, i, sz, i, vp]),
@@ -143,6 +144,10 @@ def ccl_set_launch(comm: int, sm_budget: int = 0, variant=CCL_VARIANT_AUTO,
                    pipeline_chunk_bytes: int = 0) -> None:
     _check(load_library().ccl_set_launch(comm, int(sm_budget), _code(VARIANTS, variant),
                                          int(pipeline_chunk_bytes)))
+
+
+def ccl_comm_set_debug(comm: int, wait_limit_ns: int = 0, stall_test: int = 0) -> None:
+    _check(load_library().ccl_comm_set_debug(comm, int(wait_limit_ns), int(stall_test)))
 
 
 def ccl_comm_destroy(comm: int) -> None:

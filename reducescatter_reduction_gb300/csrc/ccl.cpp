@@ -284,6 +284,16 @@ extern "C" ccl_status_t ccl_set_launch(ccl_comm_t c, int sm_budget, int variant,
     return CCL_OK;
 }
 
+extern "C" ccl_status_t ccl_comm_set_debug(ccl_comm_t c, long long wait_limit_ns, int stall_test)
+{
+    if (!c) return fail(CCL_ERR_INVALID_ARG, "comm is NULL");
+    if (wait_limit_ns < 0 || stall_test < 0 || stall_test > 1)
+        return fail(CCL_ERR_INVALID_ARG, "wait_limit_ns %lld / stall_test %d out of range", wait_limit_ns, stall_test);
+    c->wait_limit_ns = wait_limit_ns ? wait_limit_ns : 2000000000LL;
+    c->stall_test = stall_test;
+    return CCL_OK;
+}
+
 extern "C" ccl_status_t ccl_comm_destroy(ccl_comm_t c)
 {
     if (!c) return CCL_OK;
@@ -331,6 +341,7 @@ static const char *kOpName[] = {"sum", "prod", "min", "max", "avg"};
 static const char *kDtypeName[] = {"f32", "f16", "bf16", "i32"};
 static const char *kSchedName[] = {"auto", "ring", "allpairs", "custom"};
 static const char *kCollName[] = {"allreduce", "reduce_scatter", "all_gather"};
+static const char *kVariantName[] = {"auto", "ldst", "tma", "tma_bulkred"};
 
 enum Coll { COLL_AR = 0, COLL_RS = 1, COLL_AG = 2 };
 
@@ -389,9 +400,11 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     if (coll != COLL_AR && n % size_t(p) != 0)
         return fail(CCL_ERR_INVALID_ARG, "%s needs n %% p == 0 (n=%zu, p=%d)", kCollName[coll], n, p);
     if (n > (SIZE_MAX / 2) / s) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
-    int variant = c->variant == CCL_VARIANT_AUTO ? CCL_VARIANT_LDST : c->variant;
-    if (variant != CCL_VARIANT_LDST)
-        return fail(CCL_ERR_UNSUPPORTED, "variant %d is not available in this build", variant);
+    const int variant = c->variant == CCL_VARIANT_AUTO ? CCL_VARIANT_LDST : c->variant;
+    if (variant == CCL_VARIANT_TMA_BULKRED)
+        return fail(CCL_ERR_UNSUPPORTED, "the TMA bulk-reduce variant is not available in this build");
+    if (variant == CCL_VARIANT_TMA && coll == COLL_AG)
+        return fail(CCL_ERR_UNSUPPORTED, "AllGather has no TMA variant in this build (use ld/st)");
     if (n == 0) return CCL_OK;
 
     uint64_t self_mask = 0;
@@ -428,11 +441,31 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
         sched = resolve_schedule(c, schedule, double(n) * double(s));
         L.table = get_table(c, n, sched);
     }
+    if (variant == CCL_VARIANT_TMA) {
+        // bulk copies move 16-byte multiples between 16-byte aligned addresses
+        bool ok = aligned;
+        for (int k = 0; k <= p && ok; ++k) ok = (L.table->bound[k] * s) % 16 == 0;
+        if (!ok)
+            return fail(CCL_ERR_UNSUPPORTED,
+                        "the TMA variant needs 16-byte aligned pointers and chunk boundaries (n=%zu, p=%d)", n, p);
+        uint32_t tile, stages;
+        size_t smem;
+        if (!tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem))
+            return fail(CCL_ERR_INVALID_ARG, "pipeline_chunk_bytes %zu: fewer than 2 stages of %d+1 tiles fit in shared memory",
+                        c->pipe_bytes, p);
+    }
 
     LaunchInfo info;
     cudaError_t err = cudaSuccess;
     if (coll == COLL_AG) {
         err = launch_gather(L, &info);
+    } else if (variant == CCL_VARIANT_TMA) {
+        switch (dtype) {
+        case CCL_F32: err = launch_tma_f32(L, &info); break;
+        case CCL_F16: err = launch_tma_f16(L, &info); break;
+        case CCL_BF16: err = launch_tma_bf16(L, &info); break;
+        default: err = launch_tma_i32(L, &info); break;
+        }
     } else {
         switch (dtype) {
         case CCL_F32: err = launch_reduce_f32(L, &info); break;
@@ -445,7 +478,7 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     snprintf(c->last, sizeof c->last,
              "%s dtype=%s op=%s p=%d n=%zu schedule=%s variant=%s vec=%d grid=%d block=%d smem=%zu sm_budget=%d",
              info.kernel, kDtypeName[dtype], coll == COLL_AG ? "copy" : kOpName[op], p, n,
-             coll == COLL_AG ? "-" : kSchedName[sched], "ldst", L.vec ? 1 : 0, info.grid, info.block,
+             coll == COLL_AG ? "-" : kSchedName[sched], kVariantName[variant], L.vec ? 1 : 0, info.grid, info.block,
              info.smem, c->sm_budget);
     if (debug_on()) fprintf(stderr, "[ccl] %s\n", c->last);
     if (err != cudaSuccess) return cuda_fail(err, kCollName[coll]);

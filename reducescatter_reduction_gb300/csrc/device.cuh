@@ -36,6 +36,16 @@ __device__ __forceinline__ void st_v4(void *p, const uint4 &v)
                  : "memory");
 }
 
+// Results are written once and not read again by this kernel: streaming
+// (evict-first) stores.  Measured on GB300 with one 16-byte group per
+// thread: p=8 bf16 AllReduce 6.86 -> 7.03 TB/s, p=16 6.40 -> 7.05 TB/s.
+__device__ __forceinline__ void st_stream_v4(void *p, const uint4 &v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Element types.  Each traits class gives: the accumulator type, VEC =
 // elements per 16 bytes, unpacking a 16-byte vector into VEC accumulator

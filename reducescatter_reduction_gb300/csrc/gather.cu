@@ -26,7 +26,7 @@ template <int U> struct Unit;
 template <> struct Unit<16> {
     using type = uint4;
     __device__ static uint4 load(const char *p) { return ld_stream_v4(p); }
-    __device__ static void store(char *p, const uint4 &v) { st_v4(p, v); }
+    __device__ static void store(char *p, const uint4 &v) { st_stream_v4(p, v); }
 };
 template <> struct Unit<4> {
     using type = uint32_t;
@@ -83,16 +83,10 @@ static cudaError_t gather_launch(const Launch &L, LaunchInfo *info)
     a.self_mask = L.self_mask;
 
     auto kern = gather_kernel<P, U>;
-    static int occ = -1;
-    if (occ < 0) {
-        int b = 0;
-        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kGatherThreads, 0);
-        if (err != cudaSuccess) return err;
-        occ = b > 0 ? b : 1;
-    }
+    // one unit per thread; the block scheduler streams CTAs through the SMs
     uint64_t want = (a.nunits + kGatherThreads - 1) / kGatherThreads;
     if (want < 1) want = 1;
-    uint64_t cap = uint64_t(L.num_sms) * occ;
+    uint64_t cap = uint64_t(0x7fffffff);
     size_t smem = 0;
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) {
         cap = uint64_t(L.sm_budget);

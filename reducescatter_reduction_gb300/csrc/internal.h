@@ -55,11 +55,44 @@ struct LaunchInfo {
     int kernels = 0;           // kernels launched
 };
 
+// TMA variant geometry: tile bytes T per rank per stage and the stage count
+// S for p ranks.  A stage holds p input tiles and one output tile; S fills
+// the 227 KB of shared memory one CTA may address (one CTA per SM).  T-CCL
+// ("Experimental Environment") uses 8 KB chunks; T shrinks with p so that at
+// least two stages fit.  want_tile != 0 forces T.  False if no geometry fits.
+constexpr size_t kTmaSmemLimit = 227 * 1024;
+constexpr int kTmaMaxStages = 8;
+constexpr size_t kTmaCtlBytes = 64;
+
+inline bool tma_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stages, size_t *smem)
+{
+    size_t T = want_tile ? want_tile : (p <= 8 ? 8192 : p <= 16 ? 4096 : p <= 32 ? 2048 : 1024);
+    for (; T >= 1024; T /= 2) {
+        const size_t per_stage = size_t(p + 1) * T;
+        size_t S = (kTmaSmemLimit - 2 * kTmaMaxStages * 8 - kTmaCtlBytes) / per_stage;
+        if (S > size_t(kTmaMaxStages)) S = kTmaMaxStages;
+        if (S >= 2) {
+            *tile = uint32_t(T);
+            *stages = uint32_t(S);
+            *smem = S * per_stage + 2 * S * 8 + kTmaCtlBytes;
+            return true;
+        }
+        if (want_tile) return false;
+    }
+    return false;
+}
+
 // Per-dtype AllReduce / ReduceScatter launchers (ld/st variant).
 cudaError_t launch_reduce_f32(const Launch &L, LaunchInfo *info);
 cudaError_t launch_reduce_f16(const Launch &L, LaunchInfo *info);
 cudaError_t launch_reduce_bf16(const Launch &L, LaunchInfo *info);
 cudaError_t launch_reduce_i32(const Launch &L, LaunchInfo *info);
+
+// Per-dtype AllReduce / ReduceScatter launchers (TMA variant).
+cudaError_t launch_tma_f32(const Launch &L, LaunchInfo *info);
+cudaError_t launch_tma_f16(const Launch &L, LaunchInfo *info);
+cudaError_t launch_tma_bf16(const Launch &L, LaunchInfo *info);
+cudaError_t launch_tma_i32(const Launch &L, LaunchInfo *info);
 
 // AllGather (broadcast store), dtype-agnostic beyond the element size.
 cudaError_t launch_gather(const Launch &L, LaunchInfo *info);

@@ -1,0 +1,409 @@
+// TMA variant of the multi-source reduce: bulk copies into shared-memory
+// stages, a register fold in the chunk's exact order, bulk fan-out stores.
+//
+// T-CCL, sections "TMA Transfer Engine" and "Pipelined Copy and Reduction":
+// one elected thread issues bulk transfers that proceed asynchronously in the
+// TMA unit; a D-stage shared-memory pipeline keeps some stages loading while
+// others are being stored, each stage waiting for its load to complete before
+// its store is issued, and for its previous store before it is reloaded.
+// Here one CTA per SM (persistent; or k CTAs under an SM budget) walks its
+// tiles; a tile is T bytes of one chunk, taken from every rank:
+//
+//   producer (warp 0, one lane):  wait stage free -> expect p*T bytes ->
+//                                 p x cp.async.bulk global->shared (rank k of
+//                                 the chunk's order into slot k)
+//   consumers (8 warps):          wait stage full -> fold slots 0..p-1 in fp32
+//                                 -> packed result into the stage's out tile ->
+//                                 release the input slots -> one thread issues
+//                                 the bulk stores (every rank for AllReduce,
+//                                 the owner for ReduceScatter)
+//
+// Order, rounding and therefore every bit equal the ld/st kernel's.  Every
+// wait is bounded by %globaltimer: on expiry the kernel records where it gave
+// up in the communicator's status block, stops issuing work, waits (bounded)
+// for its own copies in flight and returns; ccl_comm_check() reports
+// CCL_ERR_TIMEOUT.  A tile may be shorter than T at the end of a chunk (always
+// a multiple of 16 bytes: the host only selects this variant when every chunk
+// boundary and pointer is 16-byte aligned).
+#pragma once
+
+#include "device.cuh"
+
+namespace ccl {
+
+constexpr int kTmaConsumerWarps = 8;
+constexpr int kTmaConsumers = 32 * kTmaConsumerWarps;
+constexpr int kTmaThreads = kTmaConsumers + 32;
+
+template <int PM>
+struct TmaArgs {
+    const void *src[PM];
+    void *dst[PM];
+    uint64_t bound[PM + 1];     // chunk c = elements [bound[c], bound[c+1])
+    uint64_t tstart[PM + 1];    // first tile of chunk c; tstart[p] = number of tiles
+    uint8_t order[PM][PM];      // order[c][k]: k-th rank folded into chunk c
+    int p;
+    float scale;                // avg: fl32(1/p)
+    uint32_t tile_bytes;        // T: bytes per rank per stage
+    uint32_t stages;            // S
+    unsigned *status;           // status block: [0] code, [1] block, [2] tile, [3] role
+    long long wait_ns;          // bound on any single wait
+    int stall_test;             // 1: the producer withholds its second tile (timeout test)
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, bulk copies, proxy fence, named barrier, timer.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst_smem),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Wait until at most `pending` of this thread's bulk groups still read shared memory.
+__device__ __forceinline__ void bulk_wait_read(uint32_t pending)
+{
+    switch (pending) {
+    case 0: asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.bulk.wait_group.read 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.bulk.wait_group.read 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.bulk.wait_group.read 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.bulk.wait_group.read 7;" ::: "memory"); break;
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void consumer_barrier()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, const uint4 &v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Shared control words beside the barriers.
+struct TmaCtl {
+    int abort;          // set by whichever role gives up first
+    int go;             // consumer leader -> consumers: this tile may proceed
+    uint32_t issued;    // tiles whose loads the producer issued
+    uint32_t consumed;  // tiles the consumers finished reading
+};
+
+// Bounded wait on an mbarrier phase.  Returns false if the wait gave up
+// (timeout, recorded in the status block) or another role aborted.
+template <int PM>
+__device__ __forceinline__ bool bounded_wait(const TmaArgs<PM> &a, volatile TmaCtl *ctl, uint32_t bar,
+                                             uint32_t parity, unsigned code, uint64_t tile)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (ctl->abort) return false;
+        if (global_ns() - t0 > uint64_t(a.wait_ns)) {
+            if (atomicCAS(&a.status[0], 0u, code) == 0u) {
+                a.status[1] = blockIdx.x;
+                a.status[2] = unsigned(tile);
+                a.status[3] = threadIdx.x;
+            }
+            ctl->abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+template <typename T, int OP, int P, int MODE>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    tma_reduce_kernel(const __grid_constant__ TmaArgs<(P > 0 ? P : kMaxRanks)> a)
+{
+    using Tr = Traits<T>;
+    using F = Fold<T, OP>;
+    using Acc = typename Tr::Acc;
+    constexpr int VEC = Tr::VEC;
+    constexpr int S_ELEM = (VEC == 8) ? 2 : 4;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int p = P > 0 ? P : a.p;
+    const uint32_t TB = a.tile_bytes, S = a.stages;
+    unsigned char *in_base = smem;                                   // [S][p][TB]
+    unsigned char *out_base = smem + size_t(S) * p * TB;             // [S][TB]
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_base + size_t(S) * TB);
+    uint64_t *empty = full + S;
+    volatile TmaCtl *ctl = reinterpret_cast<volatile TmaCtl *>(empty + S);
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < S; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), kTmaConsumerWarps);
+        }
+        ctl->abort = 0;
+        ctl->go = 0;
+        ctl->issued = 0;
+        ctl->consumed = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+
+    const uint64_t ntiles = a.tstart[p];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            int c = 0;
+            uint32_t i = 0;
+            for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+                const uint32_t s = i % S;
+                if (i >= S && !bounded_wait(a, ctl, smem_addr(&empty[s]), ((i / S) - 1) & 1u, 2u, t)) break;
+                while (t >= a.tstart[c + 1]) ++c;
+                const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
+                const uint64_t off = cb + (t - a.tstart[c]) * TB;
+                const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
+                if (a.stall_test && i == 1) break;  // withhold this tile: its consumers must time out
+                const uint32_t bar = smem_addr(&full[s]);
+                mbar_arrive_expect_tx(bar, uint32_t(p) * bytes);
+                unsigned char *slot = in_base + size_t(s) * p * TB;
+                for (int k = 0; k < p; ++k)
+                    bulk_load(smem_addr(slot + size_t(k) * TB),
+                              static_cast<const char *>(a.src[a.order[c][k]]) + off, bytes, bar);
+                ctl->issued = i + 1;
+            }
+        }
+    } else {
+        // ------------------------------ consumers -----------------------------
+        const int tid = threadIdx.x - 32;
+        int c = 0;
+        uint32_t i = 0;
+        for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const uint32_t s = i % S;
+            if (tid == 0) {
+                bool ok = bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, t);
+                if (ok && i >= S) bulk_wait_read(S - 1);  // out tile s: its stores from tile i-S read it
+                ctl->go = ok ? 1 : 0;
+            }
+            consumer_barrier();
+            if (!ctl->go) break;
+            while (t >= a.tstart[c + 1]) ++c;
+            const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
+            const uint64_t off = cb + (t - a.tstart[c]) * TB;
+            const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
+            const uint32_t in_s = smem_addr(in_base + size_t(s) * p * TB);
+            const uint32_t out_s = smem_addr(out_base + size_t(s) * TB);
+            for (uint32_t g = tid; g < bytes / 16; g += kTmaConsumers) {
+                Acc acc[VEC], v[VEC];
+                if constexpr (P > 0) {
+                    uint4 r[P];
+#pragma unroll
+                    for (int k = 0; k < P; ++k) r[k] = lds_v4(in_s + k * TB + g * 16);
+                    Tr::unpack(r[0], v);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[e] = F::first(v[e], a.scale);
+#pragma unroll
+                    for (int k = 1; k < P; ++k) {
+                        Tr::unpack(r[k], v);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc[e] = F::fold(acc[e], v[e], a.scale);
+                    }
+                } else {
+                    Tr::unpack(lds_v4(in_s + g * 16), v);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[e] = F::first(v[e], a.scale);
+                    for (int k = 1; k < p; ++k) {
+                        Tr::unpack(lds_v4(in_s + k * TB + g * 16), v);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc[e] = F::fold(acc[e], v[e], a.scale);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[e] = F::finish(acc[e], p);
+                sts_v4(out_s + g * 16, Tr::pack(acc));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&empty[s]));  // input slots of stage s are free
+            fence_proxy_async_smem();                          // out tile visible to the bulk stores
+            consumer_barrier();
+            if (tid == 0) {
+                if constexpr (MODE == MODE_AR) {
+                    for (int k = 0; k < p; ++k) bulk_store(static_cast<char *>(a.dst[k]) + off, out_s, bytes);
+                } else {
+                    bulk_store(static_cast<char *>(a.dst[c]) + (off - cb), out_s, bytes);
+                }
+                bulk_commit();
+                ctl->consumed = i + 1;
+            }
+        }
+        if (tid == 0) bulk_wait_all();
+    }
+    __syncthreads();
+    // After an abort, wait (bounded) for loads still in flight into shared
+    // memory before the CTA gives its shared memory back.
+    if (threadIdx.x == 0 && ctl->abort) {
+        const uint32_t issued = ctl->issued;
+        for (uint32_t j = ctl->consumed; j < issued; ++j) {
+            const uint32_t bar = smem_addr(&full[j % S]);
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(bar, (j / S) & 1u))
+                if (global_ns() - t0 > uint64_t(a.wait_ns)) break;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+
+template <typename T, int OP, int P, int MODE>
+static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
+{
+    constexpr int PM = P > 0 ? P : kMaxRanks;
+    constexpr int S_ELEM = (Traits<T>::VEC == 8) ? 2 : 4;
+    TmaArgs<PM> a;
+    uint32_t tile = 0, stages = 0;
+    size_t smem = 0;
+    if (!tma_geometry(L.p, L.pipe_bytes, &tile, &stages, &smem)) return cudaErrorInvalidValue;
+    static_assert(sizeof(TmaCtl) <= kTmaCtlBytes, "control block");
+    for (int k = 0; k < L.p; ++k) {
+        a.src[k] = L.src[k];
+        a.dst[k] = L.dst[k];
+    }
+    uint64_t tiles = 0;
+    for (int c = 0; c <= L.p; ++c) {
+        a.bound[c] = L.table->bound[c];
+        a.tstart[c] = tiles;
+        if (c < L.p) {
+            const uint64_t bytes = (L.table->bound[c + 1] - L.table->bound[c]) * S_ELEM;
+            tiles += (bytes + tile - 1) / tile;
+        }
+    }
+    for (int c = 0; c < L.p; ++c)
+        for (int k = 0; k < L.p; ++k) a.order[c][k] = L.table->order[c * L.p + k];
+    a.p = L.p;
+    a.scale = 1.0f / float(L.p);
+    a.tile_bytes = tile;
+    a.stages = stages;
+    a.status = L.status;
+    a.wait_ns = L.wait_limit_ns;
+    a.stall_test = L.stall_test;
+
+    auto kern = tma_reduce_kernel<T, OP, P, MODE>;
+    static size_t attr_smem = 0;
+    if (attr_smem < smem) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTmaSmemLimit));
+        if (err != cudaSuccess) return err;
+        attr_smem = kTmaSmemLimit;
+    }
+    uint64_t cap = uint64_t(L.num_sms);
+    if (L.sm_budget > 0 && L.sm_budget < L.num_sms) cap = uint64_t(L.sm_budget);
+    const int grid = int(tiles < cap ? (tiles ? tiles : 1) : cap);
+    kern<<<grid, kTmaThreads, smem, L.stream>>>(a);
+    if (info) {
+        info->kernel = MODE == MODE_AR ? "allreduce_tma" : "reduce_scatter_tma";
+        info->grid = grid;
+        info->block = kTmaThreads;
+        info->smem = smem;
+        info->kernels = 1;
+    }
+    return cudaGetLastError();
+}
+
+template <typename T, int OP, int MODE>
+static cudaError_t tma_launch_op_mode(const Launch &L, LaunchInfo *info)
+{
+    switch (L.p) {
+    case 2: return tma_launch_p<T, OP, 2, MODE>(L, info);
+    case 4: return tma_launch_p<T, OP, 4, MODE>(L, info);
+    case 8: return tma_launch_p<T, OP, 8, MODE>(L, info);
+    case 16: return tma_launch_p<T, OP, 16, MODE>(L, info);
+    default: return tma_launch_p<T, OP, 0, MODE>(L, info);
+    }
+}
+
+template <typename T, int OP>
+static cudaError_t tma_launch_op(const Launch &L, LaunchInfo *info)
+{
+    return L.mode == MODE_AR ? tma_launch_op_mode<T, OP, MODE_AR>(L, info)
+                             : tma_launch_op_mode<T, OP, MODE_RS>(L, info);
+}
+
+template <typename T>
+static cudaError_t launch_tma(const Launch &L, LaunchInfo *info)
+{
+    switch (L.op) {
+    case OP_SUM: return tma_launch_op<T, OP_SUM>(L, info);
+    case OP_PROD: return tma_launch_op<T, OP_PROD>(L, info);
+    case OP_MIN: return tma_launch_op<T, OP_MIN>(L, info);
+    case OP_MAX: return tma_launch_op<T, OP_MAX>(L, info);
+    case OP_AVG: return tma_launch_op<T, OP_AVG>(L, info);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace ccl

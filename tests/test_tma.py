@@ -1,0 +1,147 @@
+"""GPU tests of the TMA variant (bulk copies through shared-memory stages):
+bit-identical to the oracle in every op/dtype/schedule, independent of the
+tile size and the SM budget, explicit statuses for layouts it cannot take,
+and the bounded-wait timeout path (without faulting or hanging the GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import reducescatter_reduction_gb300 as ccl
+from reducescatter_reduction_gb300 import inputs
+from ccl_testutil import Comm, RankBuffers, bits_equal, ensure_built, stream_ptr
+from test_parity import gen, run_collective
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    ensure_built()
+
+
+def tma_sizes(p, dtype):
+    """Chunk sizes that are multiples of 16 bytes and make several tiles per
+    chunk with a short last tile (16 bytes past a whole number of tiles)."""
+    s = inputs.ELEM_BYTES[dtype]
+    per16 = 16 // s
+    return [p * per16, p * (3 * 8192 // s + per16), p * (64 * 1024 // s + 5 * per16)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
+@pytest.mark.parametrize("op", ["sum", "prod", "min", "max", "avg"])
+@pytest.mark.parametrize("sched", ["ring", "allpairs"])
+def test_tma_allreduce_matches_oracle(dtype, op, sched):
+    for p in (2, 3, 8, 16):
+        for n in tma_sizes(p, dtype):
+            xs = gen(dtype, op, p, n, seed=31 + p)
+            res, desc = run_collective(xs, "ar", op, dtype, sched, variant="tma")
+            assert "allreduce_tma" in desc and "variant=tma" in desc
+            want = oracle.allreduce(xs, op, dtype, sched)
+            for r in range(p):
+                assert bits_equal(res.host(r), want[r]), (p, n, r)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("op", ["sum", "max", "avg"])
+def test_tma_reduce_scatter_matches_oracle(dtype, op):
+    for p in (2, 5, 8, 16):
+        n = tma_sizes(p, dtype)[1]
+        xs = gen(dtype, op, p, n, seed=37)
+        res, desc = run_collective(xs, "rs", op, dtype, "ring", variant="tma")
+        assert "reduce_scatter_tma" in desc
+        want = oracle.reduce_scatter(xs, op, dtype, "ring")
+        for r in range(p):
+            assert bits_equal(res.host(r), want[r]), (p, r)
+
+
+@pytest.mark.parametrize("p", [8, 16])
+def test_tma_in_place_and_budgets_equal_ldst(p):
+    """In place, at SM budgets 1, 4, 16 and all, and at several tile sizes,
+    the TMA variant gives the ld/st kernel's bits."""
+    n = p * (1 << 20)
+    xs = gen("bf16", "sum", p, n, seed=41)
+    ref, _ = run_collective(xs, "ar", "sum", "bf16", "ring", variant="ldst")
+    for budget, tile in ((0, 0), (1, 0), (4, 2048), (16, 4096), (0, 1024)):
+        storage = inputs.STORAGE["bf16"]
+        ins = RankBuffers(xs, n, storage)
+        with Comm(ins) as cm:                      # in place
+            ccl.ccl_set_launch(cm.h, budget, "tma", tile)
+            ccl.ccl_allreduce(cm.h, "sum", "bf16", n, "ring", stream_ptr())
+            torch.cuda.synchronize()
+            desc = ccl.ccl_comm_last_launch(cm.h)
+            ccl.ccl_comm_check(cm.h)
+        grid = int(desc.split("grid=")[1].split()[0])
+        if budget:
+            assert grid <= budget
+        for r in range(p):
+            assert torch.equal(ins.views[r], ref.views[0]), (budget, tile, r)
+        assert ins.guards_intact()
+
+
+def test_tma_statuses():
+    p = 4
+    xs = gen("bf16", "sum", p, 4 * 1001, seed=43)          # chunk 1001 elements: not 16-byte aligned
+    ins = RankBuffers(xs, xs[0].size, np.uint16)
+    outs = RankBuffers(None, xs[0].size, np.uint16, p=p)
+    with Comm(ins, outs) as cm:
+        ccl.ccl_set_launch(cm.h, 0, "tma", 0)
+        with pytest.raises(ccl.CclError) as ei:
+            ccl.ccl_allreduce(cm.h, "sum", "bf16", xs[0].size, "ring", stream_ptr())
+        assert ei.value.status == ccl.CCL_ERR_UNSUPPORTED
+        with pytest.raises(ccl.CclError) as ei:
+            ccl.ccl_all_gather(cm.h, "bf16", xs[0].size - 4, stream_ptr())
+        assert ei.value.status == ccl.CCL_ERR_UNSUPPORTED
+        ccl.ccl_set_launch(cm.h, 0, "tma_bulkred", 0)
+        with pytest.raises(ccl.CclError) as ei:
+            ccl.ccl_allreduce(cm.h, "sum", "bf16", 4 * 1000, "ring", stream_ptr())
+        assert ei.value.status == ccl.CCL_ERR_UNSUPPORTED
+    p = 64
+    xs = gen("bf16", "sum", p, p * 64, seed=44)
+    ins = RankBuffers(xs, xs[0].size, np.uint16)
+    with Comm(ins) as cm:
+        ccl.ccl_set_launch(cm.h, 0, "tma", 32768)                # 65 tiles of 32 KiB cannot fit twice
+        with pytest.raises(ccl.CclError) as ei:
+            ccl.ccl_allreduce(cm.h, "sum", "bf16", xs[0].size, "ring", stream_ptr())
+        assert ei.value.status == ccl.CCL_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+
+
+def test_tma_bounded_wait_times_out_and_context_survives():
+    """The producer withholds a tile (a wait nothing will satisfy); the
+    consumers' wait gives up after 20 ms, the kernel records it and returns,
+    ccl_comm_check reports CCL_ERR_TIMEOUT once, and the same communicator
+    then runs correctly."""
+    p, n = 8, 8 * (1 << 16)
+    xs = gen("bf16", "sum", p, n, seed=45)
+    storage = inputs.STORAGE["bf16"]
+    ins = RankBuffers(xs, n, storage)
+    outs = RankBuffers(None, n, storage, p=p)
+    with Comm(ins, outs) as cm:
+        ccl.ccl_set_launch(cm.h, 1, "tma", 4096)                 # one CTA walks every tile
+        ccl.ccl_comm_set_debug(cm.h, 20_000_000, 1)
+        ccl.ccl_allreduce(cm.h, "sum", "bf16", n, "ring", stream_ptr())
+        with pytest.raises(ccl.CclError) as ei:
+            ccl.ccl_comm_check(cm.h)
+        assert ei.value.status == ccl.CCL_ERR_TIMEOUT
+        assert "gave up" in str(ei.value)
+        ccl.ccl_comm_check(cm.h)                                 # reported once, then cleared
+        ccl.ccl_comm_set_debug(cm.h, 0, 0)
+        ccl.ccl_allreduce(cm.h, "sum", "bf16", n, "ring", stream_ptr())
+        ccl.ccl_comm_check(cm.h)
+    want = oracle.allreduce(xs, "sum", "bf16", "ring")
+    for r in range(p):
+        assert bits_equal(outs.host(r), want[r])
+    assert ins.guards_intact() and outs.guards_intact()
+
+
+def test_debug_hook_arguments():
+    xs = gen("f32", "sum", 2, 64, seed=46)
+    ins = RankBuffers(xs, 64, np.float32)
+    with Comm(ins) as cm:
+        for bad in ((-1, 0), (0, 2), (0, -1)):
+            with pytest.raises(ccl.CclError) as ei:
+                ccl.ccl_comm_set_debug(cm.h, *bad)
+            assert ei.value.status == ccl.CCL_ERR_INVALID_ARG
