@@ -202,6 +202,40 @@ CCL_API ccl_status_t ccl_reduce_scatter(ccl_comm_t comm, ccl_op_t op, ccl_dtype_
  * Bytes moved: n*s read + p*n*s written (in place: (p-1)*n*s written). */
 CCL_API ccl_status_t ccl_all_gather(ccl_comm_t comm, ccl_dtype_t dtype, size_t n, void *stream);
 
+/* AllReduce for callers that cannot allocate device memory.  The pages have
+ * no counterpart: this entry point exists for code that may not call
+ * cudaMalloc -- a plug-in inside an application that owns all device memory
+ * (an inference server, a framework's memory pool), a process whose memory
+ * budget is already committed, or a latency-critical path that cannot afford
+ * cudaMalloc's implicit device synchronisation or its failure under memory
+ * pressure.  It needs no communicator and allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * Computes exactly what ccl_allreduce computes (same chunks, same orders, same
+ * bits) with the TMA variant's kernel: out_ptrs[r][e] = reduction over k of
+ * in_ptrs[k][e], e < n, for every r.  p in [1, 64]; in_ptrs / out_ptrs are host
+ * arrays of p device pointers (in place: out_ptrs[r] == in_ptrs[r]; any other
+ * overlap is CCL_ERR_INVALID_ARG); schedule is AUTO (cost model, no
+ * environment override), RING or ALLPAIRS.  The buffers and every chunk
+ * boundary must be 16-byte aligned, else CCL_ERR_UNSUPPORTED.
+ *
+ * Scratch: the kernel's only memory beyond the inputs and outputs is the
+ * status record its bounded waits write (16 bytes).  It lives in a 256-byte
+ * file-scope device array of this library (the stated maximum; a request
+ * needing more is refused with CCL_ERR_INVALID_ARG), which every GPU that loads
+ * the library holds until the process exits.  The first call on a device looks
+ * up that array's device address; make that first call before any stream
+ * capture.  All calls share the array and it keeps the last call's contents:
+ * each call first waits for the work already queued on `stream`, reads the
+ * record the previous call left (returning CCL_ERR_TIMEOUT, without
+ * launching, if a wait of that call gave up -- its outputs are then
+ * incomplete), then clears it.  Calls that overlap on the GPU (other streams,
+ * other threads) race on the record.
+ * Errors: CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED, CCL_ERR_TIMEOUT,
+ * CCL_ERR_CUDA; messages through ccl_last_error(). */
+CCL_API ccl_status_t ccl_allreduce_static(int p, void *const *in_ptrs, void *const *out_ptrs, ccl_op_t op,
+                                          ccl_dtype_t dtype, size_t n, ccl_schedule_t schedule, void *stream);
+
 /* ---------------------------------------------------------------------------
  * Host-side schedule builder and cost model (no GPU needed).
  * ------------------------------------------------------------------------- */

@@ -54,6 +54,15 @@ static ccl_status_t fail(ccl_status_t st, const char *fmt, ...)
     return st;
 }
 
+namespace ccl {
+// Lets other translation units of the library report through ccl_last_error().
+ccl_status_t record_error(ccl_status_t st, const char *msg)
+{
+    g_err = msg;
+    return st;
+}
+}  // namespace ccl
+
 static ccl_status_t cuda_fail(cudaError_t err, const char *what)
 {
     return fail(CCL_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "ccl.h"
+
 namespace ccl {
 
 constexpr int kMaxRanks = 64;
@@ -96,5 +98,8 @@ cudaError_t launch_tma_i32(const Launch &L, LaunchInfo *info);
 
 // AllGather (broadcast store), dtype-agnostic beyond the element size.
 cudaError_t launch_gather(const Launch &L, LaunchInfo *info);
+
+// Sets the message ccl_last_error() returns on this host thread; returns st.
+ccl_status_t record_error(ccl_status_t st, const char *msg);
 
 }  // namespace ccl
