@@ -64,6 +64,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-budgets", action="store_true")
     ap.add_argument("--n", type=int, default=N,
                     help="bf16 elements per rank (default 2^27; smaller only for profiling runs)")
     return ap.parse_args(argv)
@@ -333,6 +334,9 @@ def run_ours(args, dist: Dist):
         del outs
         torch.cuda.empty_cache()
         result["sweep"] = run_sweep(dist, dev, sptr, stream, peak, l2, ins)
+    if not args.no_budgets:
+        torch.cuda.empty_cache()
+        result["sm_budgets"] = run_budgets(dev, sptr, stream, peak)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline_from(ins)
     del ins
@@ -341,40 +345,93 @@ def run_ours(args, dist: Dist):
 
 
 def run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes, n):
-    """Same metric with host buffers: every step copies the p inputs from
-    pinned host memory, runs the AllReduce and copies the p results back."""
+    """Same metric with host buffers: every step copies its p inputs from
+    pinned host memory, runs the AllReduce through the C ABI, and copies its
+    p results back to pinned host memory, all inside the timed region.
+
+    value: a stream of such steps, double-buffered (two device buffer sets;
+    host->device copies on one stream, AllReduce on another, device->host on a
+    third, ordered by events), so that step i+1's input copy overlaps step i's
+    AllReduce and output copy.  serial: one step at a time on one stream."""
     import torch
     import reducescatter_reduction_gb300 as ccl
 
     h_in = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
-    h_out = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
     for h, d in zip(h_in, ins):
         h.copy_(d)
+    h_out = [[torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)] for _ in range(2)]
+    ins2 = [torch.empty_like(t) for t in ins]
+    outs2 = [torch.empty_like(t) for t in outs]
+    comm2 = ccl.ccl_comm_create(P, [t.data_ptr() for t in ins2])
+    ccl.ccl_comm_set_outputs(comm2, [t.data_ptr() for t in outs2])
+    sets = [(comm, ins, outs), (comm2, ins2, outs2)]
 
-    def step():
+    def timed(fn, steps):
+        for i in range(2):
+            fn(i)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        start_stream = torch.cuda.current_stream()
+        for i in range(steps):
+            fn(i)
+        end_stream = last_stream[0] or start_stream
+        e1.record(end_stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        return e0.elapsed_time(e1)
+
+    last_stream = [None]
+
+    def serial_step(i):
         for h, d in zip(h_in, ins):
             d.copy_(h, non_blocking=True)
         ccl.ccl_allreduce(comm, "sum", "bf16", n, args.schedule, sptr)
-        for h, d in zip(h_out, outs):
+        for h, d in zip(h_out[0], outs):
             h.copy_(d, non_blocking=True)
 
-    for _ in range(2):
-        step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    dist.barrier()
-    t_ms, _, gbs = aggregate(dist, e0.elapsed_time(e1), alg_bytes * args.e2e_steps)
+    s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_h2d = [torch.cuda.Event() for _ in range(2)]
+    ev_ar = [torch.cuda.Event() for _ in range(2)]
+    ev_d2h = [torch.cuda.Event() for _ in range(2)]
+    issued = [False, False]
+
+    def piped_step(i):
+        k = i % 2
+        h, d_in, d_out = sets[k]
+        s_h2d.wait_stream(stream) if i == 0 else None
+        if issued[k]:
+            s_h2d.wait_event(ev_ar[k])            # the AllReduce two steps back read d_in
+        with torch.cuda.stream(s_h2d):
+            for hh, dd in zip(h_in, d_in):
+                dd.copy_(hh, non_blocking=True)
+        ev_h2d[k].record(s_h2d)
+        stream.wait_event(ev_h2d[k])
+        if issued[k]:
+            stream.wait_event(ev_d2h[k])          # the output copy two steps back read d_out
+        ccl.ccl_allreduce(h, "sum", "bf16", n, args.schedule, sptr)
+        ev_ar[k].record(stream)
+        s_d2h.wait_event(ev_ar[k])
+        with torch.cuda.stream(s_d2h):
+            for hh, dd in zip(h_out[k], d_out):
+                hh.copy_(dd, non_blocking=True)
+        ev_d2h[k].record(s_d2h)
+        issued[k] = True
+        last_stream[0] = s_d2h
+
+    t_serial = timed(serial_step, args.e2e_steps)
+    last_stream[0] = None
+    t_piped = timed(piped_step, args.e2e_steps)
+    ccl.ccl_comm_destroy(comm2)
+    t_ms, _, gbs = aggregate(dist, t_piped, alg_bytes * args.e2e_steps)
+    ts_ms, _, gbs_serial = aggregate(dist, t_serial, alg_bytes * args.e2e_steps)
     return {"value": round(gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": P * n * S,
             "d2h_bytes_per_step": P * n * S, "steps": args.e2e_steps,
-            "ms_per_step": round(t_ms / args.e2e_steps, 4)}
+            "ms_per_step": round(t_ms / args.e2e_steps, 4),
+            "mode": "double-buffered: H2D, AllReduce and D2H on three streams",
+            "serial": {"value": round(gbs_serial, 2), "ms_per_step": round(ts_ms / args.e2e_steps, 4)}}
 
 
 def run_rs_ag(args, ins, outs, sptr, stream, peak, n):
@@ -410,6 +467,76 @@ def run_rs_ag(args, ins, outs, sptr, stream, peak, n):
     ccl.ccl_comm_destroy(rs)
     ccl.ccl_comm_destroy(ag)
     return rows
+
+
+def run_budgets(dev, sptr, stream, peak):
+    """MoE hidden-state AllReduce, p=16 bf16 [16384, 7168] per rank (224 MiB,
+    3.5 GiB in + 3.5 GiB out), ring, at SM budgets from 4 SMs to the whole GPU,
+    ld/st and TMA variants (T-CCL's restricted-CTA-budget comparison)."""
+    import torch
+    import reducescatter_reduction_gb300 as ccl
+
+    p, n = 16, 16384 * 7168
+    nbytes = 2 * p * n * S
+    ins = [torch.randn(n, device=dev, dtype=torch.float32).to(torch.bfloat16) for _ in range(p)]
+    outs = [torch.empty_like(t) for t in ins]
+    h = ccl.ccl_comm_create(p, [t.data_ptr() for t in ins])
+    ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rows = []
+    for variant in ("ldst", "tma"):
+        for budget in (4, 8, 16, 32, 76, 0):
+            ccl.ccl_set_launch(h, budget, variant, 0)
+            for _ in range(2):
+                ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", sptr)
+            torch.cuda.synchronize()
+            iters = 3 if budget and budget <= 16 else 10
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(iters):
+                ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", sptr)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / iters
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            used = budget or sms
+            rows.append({"variant": variant, "sm_budget": budget or "all", "ms": round(ms, 3),
+                         "GBps": round(gbs, 1), "GBps_per_SM": round(gbs / used, 2),
+                         "frac_of_hbm_peak": round(gbs / peak, 4),
+                         "launch": ccl.ccl_comm_last_launch(h)})
+    ccl.ccl_comm_check(h)
+    ccl.ccl_comm_destroy(h)
+    del ins, outs
+    torch.cuda.empty_cache()
+    return rows
+
+
+def graph_latency(comms, sets, n, sched, calls=200):
+    """Per-call device time with the host out of the way: `calls` AllReduces
+    (rotating buffer sets) captured in one CUDA graph and replayed."""
+    import torch
+    import reducescatter_reduction_gb300 as ccl
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            cs = torch.cuda.current_stream().cuda_stream
+            for i in range(calls):
+                ccl.ccl_allreduce(comms[i % sets], "sum", "bf16", n, sched, cs)
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (5 * calls)
 
 
 def run_sweep(dist, dev, sptr, stream, peak, l2, big_inputs):
@@ -453,6 +580,8 @@ def run_sweep(dist, dev, sptr, stream, peak, l2, big_inputs):
             gbs = per_set / (us * 1e-6) / 1e9
             row[sched] = {"us": round(us, 3), "GBps": round(gbs, 1),
                           "frac_of_hbm_peak": round(gbs / peak, 4) if per_set >= 4 * l2 else None}
+            if n * S <= (4 << 20):
+                row[sched]["us_graph"] = round(graph_latency(comms, sets, n, sched), 3)
         rows.append(row)
         for h in comms:
             ccl.ccl_comm_destroy(h)

@@ -424,3 +424,55 @@ def test_moe_p16_sm_budgets():
         assert outs.guards_intact()
         del outs
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("variant", ["ldst", "tma"])
+def test_cuda_graph_capture_and_replay(variant):
+    """The collective calls only check arguments and enqueue kernels, so they
+    can be captured in a CUDA graph; replays recompute from the current input
+    contents."""
+    p, n, dtype = 8, 8 * 65536, "bf16"
+    xs = gen(dtype, "sum", p, n, seed=50)
+    ys = gen(dtype, "sum", p, n, seed=51)
+    storage = inputs.STORAGE[dtype]
+    ins = RankBuffers(xs, n, storage)
+    outs = RankBuffers(None, n, storage, p=p)
+    rs_out = RankBuffers(None, n // p, storage, p=p)
+    with Comm(ins, outs) as cm, Comm(ins, rs_out) as cm_rs:
+        ccl.ccl_set_launch(cm.h, 0, variant, 0)
+        ccl.ccl_set_launch(cm_rs.h, 0, variant, 0)
+        ccl.ccl_allreduce(cm.h, "sum", dtype, n, "ring", stream_ptr())      # first use: kernel attributes
+        ccl.ccl_reduce_scatter(cm_rs.h, "sum", dtype, n, "ring", stream_ptr())
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                s = torch.cuda.current_stream().cuda_stream
+                ccl.ccl_allreduce(cm.h, "sum", dtype, n, "ring", s)
+                ccl.ccl_reduce_scatter(cm_rs.h, "sum", dtype, n, "ring", s)
+        torch.cuda.current_stream().wait_stream(side)
+        for src in (xs, ys):
+            for r in range(p):
+                ins.views[r].copy_(torch.from_numpy(src[r].view(np.uint8)).to("cuda"))
+            g.replay()
+            torch.cuda.synchronize()
+            want = oracle.allreduce(src, "sum", dtype, "ring")
+            want_rs = oracle.reduce_scatter(src, "sum", dtype, "ring")
+            for r in range(p):
+                assert bits_equal(outs.host(r), want[r])
+                assert bits_equal(rs_out.host(r), want_rs[r])
+        ccl.ccl_comm_check(cm.h)
+
+
+def test_auto_variant_follows_sm_budget():
+    p, n = 16, 16 * 65536
+    xs = gen("bf16", "sum", p, n, seed=52)
+    _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto")
+    assert "variant=ldst" in desc
+    _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
+    assert "variant=tma" in desc and "grid=16" in desc
+    xs = gen("bf16", "sum", 4, 4 * 1001, seed=53)       # chunks off the 16-byte grid: ld/st
+    _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
+    assert "variant=ldst" in desc
