@@ -328,6 +328,7 @@ def run_ours(args, dist: Dist):
         result["e2e"] = run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes, n)
     if not args.no_sweep:
         result["rs_ag"] = run_rs_ag(args, ins, outs, sptr, stream, peak, n)
+        result["variants"] = run_variants(comm, sptr, stream, peak, n, args)
 
     ccl.ccl_comm_destroy(comm)
     if not args.no_sweep:
@@ -434,6 +435,36 @@ def run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes, n):
             "serial": {"value": round(gbs_serial, 2), "ms_per_step": round(ts_ms / args.e2e_steps, 4)}}
 
 
+def run_variants(comm, sptr, stream, peak, n, args):
+    """The benchmark AllReduce through each kernel variant (all SMs).  GB/s
+    counts the AllReduce's algorithmic bytes 2*p*n*s for all of them; the
+    bulk-reduce variant moves 2*(p+1)*n*s (ReduceScatter then AllGather)."""
+    import torch
+    import reducescatter_reduction_gb300 as ccl
+
+    rows = {}
+    for variant in ("ldst", "tma", "tma_bulkred"):
+        ccl.ccl_set_launch(comm, 0, variant, 0)
+        for _ in range(3):
+            ccl.ccl_allreduce(comm, "sum", "bf16", n, "ring", sptr)
+        torch.cuda.synchronize()
+        iters = 50
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            ccl.ccl_allreduce(comm, "sum", "bf16", n, "ring", sptr)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / iters
+        gbs = 2 * P * n * S / (us * 1e-6) / 1e9
+        rows[variant] = {"us": round(us, 1), "GBps": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+                         "launch": ccl.ccl_comm_last_launch(comm)}
+    ccl.ccl_set_launch(comm, args.sm_budget, args.variant, 0)
+    ccl.ccl_comm_check(comm)
+    return rows
+
+
 def run_rs_ag(args, ins, outs, sptr, stream, peak, n):
     """The same buffers as separate ReduceScatter (out[r] = chunk r) and
     AllGather (in place): GB/s over each one's algorithmic bytes."""
@@ -484,7 +515,7 @@ def run_budgets(dev, sptr, stream, peak):
     ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     rows = []
-    for variant in ("ldst", "tma"):
+    for variant in ("ldst", "tma", "tma_bulkred"):
         for budget in (4, 8, 16, 32, 76, 0):
             ccl.ccl_set_launch(h, budget, variant, 0)
             for _ in range(2):

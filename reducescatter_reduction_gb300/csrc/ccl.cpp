@@ -428,10 +428,13 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
             if (ok && tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem)) variant = CCL_VARIANT_TMA;
         }
     }
-    if (variant == CCL_VARIANT_TMA_BULKRED)
-        return fail(CCL_ERR_UNSUPPORTED, "the TMA bulk-reduce variant is not available in this build");
-    if (variant == CCL_VARIANT_TMA && coll == COLL_AG)
+    if ((variant == CCL_VARIANT_TMA || variant == CCL_VARIANT_TMA_BULKRED) && coll == COLL_AG)
         return fail(CCL_ERR_UNSUPPORTED, "AllGather has no TMA variant in this build (use ld/st)");
+    if (variant == CCL_VARIANT_TMA_BULKRED && !bulkred_supported(dtype, op))
+        return fail(CCL_ERR_UNSUPPORTED,
+                    "the bulk-reduce variant has sum (f32/f16/bf16/i32) and min/max (f16/bf16/i32) only");
+    if (variant == CCL_VARIANT_TMA_BULKRED && coll == COLL_AR && n % size_t(p) != 0)
+        return fail(CCL_ERR_UNSUPPORTED, "the bulk-reduce AllReduce needs n %% p == 0 (n=%zu, p=%d)", n, p);
     if (n == 0) return CCL_OK;
 
     uint64_t self_mask = 0;
@@ -468,7 +471,7 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
         sched = resolve_schedule(c, schedule, double(n) * double(s));
         L.table = get_table(c, n, sched);
     }
-    if (variant == CCL_VARIANT_TMA) {
+    if (variant == CCL_VARIANT_TMA || variant == CCL_VARIANT_TMA_BULKRED) {
         // bulk copies move 16-byte multiples between 16-byte aligned addresses
         bool ok = aligned;
         for (int k = 0; k <= p && ok; ++k) ok = (L.table->bound[k] * s) % 16 == 0;
@@ -477,7 +480,9 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
                         "the TMA variant needs 16-byte aligned pointers and chunk boundaries (n=%zu, p=%d)", n, p);
         uint32_t tile, stages;
         size_t smem;
-        if (!tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem))
+        const bool fits = variant == CCL_VARIANT_TMA ? tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem)
+                                                     : bulkred_geometry(p, c->pipe_bytes, &tile, &stages, &smem);
+        if (!fits)
             return fail(CCL_ERR_INVALID_ARG, "pipeline_chunk_bytes %zu: fewer than 2 stages of %d+1 tiles fit in shared memory",
                         c->pipe_bytes, p);
     }
@@ -492,6 +497,23 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
         case CCL_F16: err = launch_tma_f16(L, &info); break;
         case CCL_BF16: err = launch_tma_bf16(L, &info); break;
         default: err = launch_tma_i32(L, &info); break;
+        }
+    } else if (variant == CCL_VARIANT_TMA_BULKRED) {
+        switch (dtype) {
+        case CCL_F32: err = launch_bulkred_f32(L, &info); break;
+        case CCL_F16: err = launch_bulkred_f16(L, &info); break;
+        case CCL_BF16: err = launch_bulkred_bf16(L, &info); break;
+        default: err = launch_bulkred_i32(L, &info); break;
+        }
+        if (err == cudaSuccess && coll == COLL_AR) {
+            // every chunk now sits in its owner's output: broadcast it in place
+            Launch G = L;
+            for (int r = 0; r < p; ++r) G.src[r] = L.dst[r];
+            G.self_mask = (p == 64) ? ~uint64_t(0) : ((uint64_t(1) << p) - 1);
+            G.vec = aligned && (n / p * s) % 16 == 0;
+            LaunchInfo ginfo;
+            err = launch_gather(G, &ginfo);
+            info.kernels += ginfo.kernels;
         }
     } else {
         switch (dtype) {

@@ -84,6 +84,34 @@ inline bool tma_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stag
     return false;
 }
 
+// Bulk-reduce variant: the reductions the PTX bulk-reduce instruction
+// provides (sum on f32/f16/bf16/i32, min/max on f16/bf16/i32), and its
+// geometry: two stages of p tiles, small enough for several CTAs per SM.
+inline bool bulkred_supported(int dtype, int op)
+{
+    if (op == OP_SUM) return true;
+    if (op == OP_MIN || op == OP_MAX) return dtype != DT_F32;
+    return false;
+}
+
+inline bool bulkred_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stages, size_t *smem)
+{
+    // default: about 64 KB per CTA, so that three CTAs share an SM
+    size_t T = want_tile ? want_tile : (p <= 4 ? 8192 : p <= 8 ? 4096 : p <= 16 ? 2048 : 1024);
+    const uint32_t S = 2;
+    for (; T >= 1024; T /= 2) {
+        const size_t bytes = size_t(S) * p * T + 2 * S * 8 + kTmaCtlBytes;
+        if (bytes <= kTmaSmemLimit) {
+            *tile = uint32_t(T);
+            *stages = S;
+            *smem = bytes;
+            return true;
+        }
+        if (want_tile) return false;
+    }
+    return false;
+}
+
 // Per-dtype AllReduce / ReduceScatter launchers (ld/st variant).
 cudaError_t launch_reduce_f32(const Launch &L, LaunchInfo *info);
 cudaError_t launch_reduce_f16(const Launch &L, LaunchInfo *info);
@@ -95,6 +123,14 @@ cudaError_t launch_tma_f32(const Launch &L, LaunchInfo *info);
 cudaError_t launch_tma_f16(const Launch &L, LaunchInfo *info);
 cudaError_t launch_tma_bf16(const Launch &L, LaunchInfo *info);
 cudaError_t launch_tma_i32(const Launch &L, LaunchInfo *info);
+
+// Per-dtype bulk-reduce launchers: the ReduceScatter core (for MODE_AR chunk c
+// is written into rank c's output at the chunk's offset; the caller then runs
+// the in-place AllGather).
+cudaError_t launch_bulkred_f32(const Launch &L, LaunchInfo *info);
+cudaError_t launch_bulkred_f16(const Launch &L, LaunchInfo *info);
+cudaError_t launch_bulkred_bf16(const Launch &L, LaunchInfo *info);
+cudaError_t launch_bulkred_i32(const Launch &L, LaunchInfo *info);
 
 // AllGather (broadcast store), dtype-agnostic beyond the element size.
 cudaError_t launch_gather(const Launch &L, LaunchInfo *info);

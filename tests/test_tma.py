@@ -95,8 +95,8 @@ def test_tma_statuses():
             ccl.ccl_all_gather(cm.h, "bf16", xs[0].size - 4, stream_ptr())
         assert ei.value.status == ccl.CCL_ERR_UNSUPPORTED
         ccl.ccl_set_launch(cm.h, 0, "tma_bulkred", 0)
-        with pytest.raises(ccl.CclError) as ei:
-            ccl.ccl_allreduce(cm.h, "sum", "bf16", 4 * 1000, "ring", stream_ptr())
+        with pytest.raises(ccl.CclError) as ei:                   # a product has no bulk reduction
+            ccl.ccl_allreduce(cm.h, "prod", "bf16", 4 * 1000, "ring", stream_ptr())
         assert ei.value.status == ccl.CCL_ERR_UNSUPPORTED
     p = 64
     xs = gen("bf16", "sum", p, p * 64, seed=44)
@@ -145,3 +145,96 @@ def test_debug_hook_arguments():
             with pytest.raises(ccl.CclError) as ei:
                 ccl.ccl_comm_set_debug(cm.h, *bad)
             assert ei.value.status == ccl.CCL_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------------------
+# bulk-reduce variant: reductions applied by the memory system
+# ---------------------------------------------------------------------------
+
+EPS_OUT = {"f32": 2.0 ** -23, "f16": 2.0 ** -10, "bf16": 2.0 ** -7}
+
+
+def decode(arr, dtype):
+    if dtype == "f32":
+        return arr.astype(np.float64)
+    if dtype == "f16":
+        return arr.view(np.float16).astype(np.float64)
+    return torch.from_numpy(arr.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+
+
+def within_reassociation_bound(got, xs, dtype):
+    """|y - exact| <= 2 p eps_out sum_k |x_k| per element (exact in fp64)."""
+    p = len(xs)
+    xf = np.stack([decode(x, dtype) for x in xs])
+    exact = xf.sum(axis=0)
+    bound = 2 * p * EPS_OUT[dtype] * np.abs(xf).sum(axis=0)
+    err = np.abs(decode(got, dtype) - exact)
+    return bool(np.all(err <= bound)), float(np.max(err / np.maximum(bound, 1e-300)))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("p", [2, 8, 16])
+def test_bulkred_allreduce_sum_within_bound(dtype, p):
+    n = tma_sizes(p, dtype)[2]
+    xs = gen(dtype, "sum", p, n, seed=80 + p)
+    res, desc = run_collective(xs, "ar", "sum", dtype, "ring", variant="tma_bulkred")
+    assert "allreduce_tma_bulkred" in desc
+    ok, worst = within_reassociation_bound(res.host(0), xs, dtype)
+    assert ok, worst
+    assert res.identical_across_ranks()
+
+
+@pytest.mark.parametrize("dtype,op", [("i32", "sum"), ("i32", "min"), ("i32", "max"),
+                                      ("f16", "min"), ("f16", "max"), ("bf16", "min"), ("bf16", "max")])
+def test_bulkred_exact_ops_match_oracle(dtype, op):
+    """Integer sums and min/max are exact in any order: bit-identical."""
+    for p in (4, 8, 16):
+        n = tma_sizes(p, dtype)[1]
+        xs = gen(dtype, op, p, n, seed=90 + p)
+        res, _ = run_collective(xs, "ar", op, dtype, "ring", variant="tma_bulkred")
+        want = oracle.allreduce(xs, op, dtype, "ring")
+        for r in range(p):
+            assert bits_equal(res.host(r), want[r]), (p, r)
+        rs, desc = run_collective(xs, "rs", op, dtype, "allpairs", variant="tma_bulkred")
+        assert "reduce_scatter_tma_bulkred" in desc
+        want = oracle.reduce_scatter(xs, op, dtype, "allpairs")
+        for r in range(p):
+            assert bits_equal(rs.host(r), want[r]), (p, r)
+
+
+def test_bulkred_reduce_scatter_in_place_and_budget():
+    p, dtype = 8, "bf16"
+    n = p * (1 << 18)
+    xs = gen(dtype, "sum", p, n, seed=95)
+    storage = inputs.STORAGE[dtype]
+    ins = RankBuffers(xs, n, storage)
+    chunk = n // p
+    with Comm(ins, out_ptrs=[ins.ptr(r, r * chunk) for r in range(p)]) as cm:
+        ccl.ccl_set_launch(cm.h, 8, "tma_bulkred", 0)
+        ccl.ccl_reduce_scatter(cm.h, "sum", dtype, n, "ring", stream_ptr())
+        torch.cuda.synchronize()
+        desc = ccl.ccl_comm_last_launch(cm.h)
+        ccl.ccl_comm_check(cm.h)
+    assert int(desc.split("grid=")[1].split()[0]) <= 8
+    for r in range(p):
+        got = ins.host(r)[r * chunk:(r + 1) * chunk]
+        ok, worst = within_reassociation_bound(got, [x[r * chunk:(r + 1) * chunk] for x in xs], dtype)
+        assert ok, (r, worst)
+    assert ins.guards_intact()
+
+
+def test_bulkred_statuses():
+    p = 8
+    xs = gen("f32", "sum", p, p * 64, seed=96)
+    ins = RankBuffers(xs, p * 64, np.float32)
+    outs = RankBuffers(None, p * 64, np.float32, p=p)
+    with Comm(ins, outs) as cm:
+        ccl.ccl_set_launch(cm.h, 0, "tma_bulkred", 0)
+        for op, dtype in (("prod", "f32"), ("avg", "f32"), ("min", "f32"), ("max", "f32")):
+            with pytest.raises(ccl.CclError) as ei:
+                ccl.ccl_allreduce(cm.h, op, dtype, p * 64, "ring", stream_ptr())
+            assert ei.value.status == ccl.CCL_ERR_UNSUPPORTED
+        with pytest.raises(ccl.CclError) as ei:                   # n % p != 0
+            ccl.ccl_allreduce(cm.h, "sum", "f32", p * 64 - 4, "ring", stream_ptr())
+        assert ei.value.status == ccl.CCL_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
