@@ -59,6 +59,7 @@ def lib():
         L.oracle_reduce_scatter.argtypes = [i32, u64, i32, i32, i32, pp, pp]
         L.oracle_all_gather.argtypes = [i32, u64, i32, pp, pp]
         L.oracle_allreduce_orders.argtypes = [i32, u64, i32, i32, ctypes.POINTER(ctypes.c_uint8), pp, pp]
+        L.oracle_allreduce_ring_stepwise.argtypes = [i32, u64, i32, i32, pp, pp]
         L.oracle_allreduce_at.argtypes = [i32, u64, i32, i32, i32, pp,
                                           ctypes.POINTER(u64), u64, vp]
         L.oracle_chunk_bounds.argtypes = [i32, u64, i32, ctypes.POINTER(u64), ctypes.POINTER(u64)]
@@ -121,6 +122,17 @@ def allreduce_orders(xs, op, dtype, order):
     ys = [np.empty(n, dtype=NP_STORAGE[dt]) for _ in xs]
     if lib().oracle_allreduce_orders(p, n, dt, o, arr, _ptrs(xs), _ptrs(ys)):
         raise ValueError("oracle_allreduce_orders rejected its arguments")
+    return ys
+
+
+def allreduce_ring_stepwise(xs, op, dtype):
+    """The ring run hop by hop, partials held in the element type between hops."""
+    dt, o = _code(DTYPES, dtype), _code(OPS, op)
+    _check_inputs(xs, dt)
+    n = xs[0].size
+    ys = [np.empty(n, dtype=NP_STORAGE[dt]) for _ in xs]
+    if lib().oracle_allreduce_ring_stepwise(len(xs), n, dt, o, _ptrs(xs), _ptrs(ys)):
+        raise ValueError("oracle_allreduce_ring_stepwise rejected its arguments")
     return ys
 
 

@@ -254,6 +254,73 @@ int oracle_allreduce(int p, uint64_t n, int dtype, int op, int schedule,
     return oracle_allreduce_orders(p, n, dtype, op, order, x, y);
 }
 
+/* AllReduce as the ring runs it hop by hop ("Inside NCCL AllReduce", "The
+ * ring, exactly as the kernel runs it"): chunk c starts as rank (c+1)'s
+ * contribution; at each of the p-1 reduce-scatter hops the next rank adds its
+ * own contribution to the partial it received and passes it on.  Between hops
+ * a partial lives in a rank buffer, so it is held in the element type: each
+ * hop widens the received partial and the local contribution to fp32 (avg:
+ * contributions pre-scaled by fl32(1/p) as read), applies the op once and
+ * rounds the result back to the element type.  The finished chunk then
+ * circulates unchanged (all-gather half).  int32 and fp32 give the same bits as
+ * oracle_allreduce with the ring schedule; fp16/bf16 round at every hop. */
+int oracle_allreduce_ring_stepwise(int p, uint64_t n, int dtype, int op, const void *const *x, void *const *y)
+{
+    if (check_args(p, dtype, op, OR_RING)) return -1;
+    size_t s = (dtype == OR_F32 || dtype == OR_I32) ? 4 : 2;
+    float scale = 1.0f / (float)p;
+    for (int c = 0; c < p; ++c) {
+        uint64_t b, en;
+        oracle_chunk_bounds(p, n, c, &b, &en);
+        for (uint64_t e = b; e < en; ++e) {
+            int first = (c + 1) % p;
+            unsigned char held[4];                    /* the partial, in the element type */
+            if (dtype == OR_I32) {
+                memcpy(held, (const char *)x[first] + e * s, 4);
+            } else {
+                float v = load_f(dtype, x[first], e);
+                if (op == OR_AVG) v = v * scale;
+                store_f(dtype, held, 0, v);
+            }
+            for (int hop = 1; hop < p; ++hop) {
+                int d = (c + 1 + hop) % p;
+                if (dtype == OR_I32) {
+                    uint32_t acc, v;
+                    memcpy(&acc, held, 4);
+                    v = ((const uint32_t *)x[d])[e];
+                    int32_t sa = (int32_t)acc, sv = (int32_t)v;
+                    switch (op) {
+                    case OR_SUM: case OR_AVG: acc = acc + v; break;
+                    case OR_PROD: acc = acc * v; break;
+                    case OR_MIN: acc = (sv < sa) ? v : acc; break;
+                    case OR_MAX: acc = (sv > sa) ? v : acc; break;
+                    }
+                    memcpy(held, &acc, 4);
+                } else {
+                    float acc = load_f(dtype, held, 0);
+                    float v = load_f(dtype, x[d], e);
+                    switch (op) {
+                    case OR_SUM: acc = acc + v; break;
+                    case OR_AVG: acc = acc + v * scale; break;
+                    case OR_PROD: acc = acc * v; break;
+                    case OR_MIN: acc = (v < acc) ? v : acc; break;
+                    case OR_MAX: acc = (v > acc) ? v : acc; break;
+                    }
+                    store_f(dtype, held, 0, acc);
+                }
+            }
+            if (dtype == OR_I32 && op == OR_AVG) {
+                int32_t r;
+                memcpy(&r, held, 4);
+                r = r / p;                            /* divided once, at the end */
+                memcpy(held, &r, 4);
+            }
+            for (int k = 0; k < p; ++k) memcpy((char *)y[k] + e * s, held, s);
+        }
+    }
+    return 0;
+}
+
 /* ReduceScatter: rank r's output y[r] receives chunk r of the reduction,
  * n/p elements written from offset 0.  Requires n % p == 0. */
 int oracle_reduce_scatter(int p, uint64_t n, int dtype, int op, int schedule,

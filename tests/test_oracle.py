@@ -519,3 +519,62 @@ def test_cost_model_worked_example():
         else:
             hi = mid
     assert round(lo / 2 ** 20, 1) == float(g["crossover_MiB"][0])
+
+
+# ---------------------------------------------------------------------------
+# the ring run hop by hop (partials in the element type)
+# ---------------------------------------------------------------------------
+
+def test_ring_stepwise_worked_case():
+    rows = {r[0]: [float(v) for v in r[1:]] for r in read_golden("ring_stepwise_bf16_p3.txt")}
+    xs = [to_storage(rows[f"rank{k}"], "bf16") for k in range(3)]
+    step = as_float(oracle.allreduce_ring_stepwise(xs, "sum", "bf16")[0], "bf16")
+    fused = as_float(oracle.allreduce(xs, "sum", "bf16", "ring")[0], "bf16")
+    assert step.tolist() == rows["stepwise"]
+    assert fused.tolist() == rows["fused"]
+
+
+@pytest.mark.parametrize("fixture,p", [("ring_order_p3.txt", 3), ("ring_order_p4.txt", 4),
+                                       ("ring_order_p8.txt", 8)])
+def test_ring_stepwise_order_pin(fixture, p):
+    """fp32 partials are fp32 either way, so the absorption probe sees the
+    page's ring order through the stepwise path too."""
+    expected = golden_orders(fixture)
+    triples, n, xs = _triple_probe(p, "f32")
+    T = len(triples)
+    y = oracle.allreduce_ring_stepwise(xs, "sum", "f32")[0]
+    for c in range(p):
+        got = y[c * T:(c + 1) * T] != 0
+        want = np.array([_survives(expected[c], *t) for t in triples])
+        assert np.array_equal(got, want), f"chunk {c}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("p", [2, 5, 8, 16])
+def test_ring_stepwise_rounds_each_hop(dtype, p):
+    """Each hop rounds once to the element type: the error stays within
+    (p-1) roundings of |partial| <= sum|x| (u_out each) plus fp32 terms, and
+    small-integer inputs (exact at every hop) give the exact sum."""
+    n = 2048
+    xs = [inputs.normal(n, 30, r, 1.0, dtype) for r in range(p)]
+    xf = np.stack([as_float(x, dtype) for x in xs])
+    y = as_float(oracle.allreduce_ring_stepwise(xs, "sum", dtype)[0], dtype)
+    exact, absum = xf.sum(axis=0), np.abs(xf).sum(axis=0)
+    assert np.all(np.abs(y - exact) <= (p - 1) * U_OUT[dtype] * absum * 1.001 + SUB_ABS[dtype] * p)
+    ints = [to_storage(np.random.default_rng(r).integers(-8, 9, n), dtype) for r in range(p)]
+    y = as_float(oracle.allreduce_ring_stepwise(ints, "sum", dtype)[0], dtype)
+    assert np.array_equal(y, np.stack([as_float(x, dtype) for x in ints]).sum(axis=0))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+@pytest.mark.parametrize("op", ["sum", "prod", "min", "max", "avg"])
+def test_ring_stepwise_wide_types_match_fused(dtype, op):
+    """fp32 and int32 partials lose nothing between hops: same bits as the
+    fused ring fold (and the int32 closed forms)."""
+    p, n = 8, 999
+    xs = inputs.coverage(op, dtype, n=n, p=p) if dtype == "i32" else [
+        inputs.normal(n, 31, r, 1.0, dtype) for r in range(p)]
+    a = oracle.allreduce_ring_stepwise(xs, op, dtype)
+    b = oracle.allreduce(xs, op, dtype, "ring")
+    for r in range(p):
+        assert np.array_equal(a[r].view(np.uint8), b[r].view(np.uint8))

@@ -395,7 +395,8 @@ def test_op_coverage_64M(dtype, ops):
 
 def test_moe_p16_sm_budgets():
     """p=16 bf16 [16384, 7168] per rank (224 MiB each), ring: sampled oracle
-    comparison, and the same bits at SM budgets 4, 8, 16 and all."""
+    comparison, and the same bits from the ld/st and TMA variants at SM
+    budgets 4, 8, 16 and all; the bulk-reduce variant within its bound."""
     p, dtype = 16, "bf16"
     xs = inputs.moe(p)
     n = xs[0].size
@@ -403,12 +404,16 @@ def test_moe_p16_sm_budgets():
     want = oracle.allreduce_at(xs, idx, "sum", dtype, "ring")
     storage = inputs.STORAGE[dtype]
     ins = RankBuffers(xs, n, storage)
+    xf = np.stack([x[idx.astype(np.int64)] for x in xs])
+    xf = torch.from_numpy(xf.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    exact, bound = xf.sum(axis=0), 2 * p * 2.0 ** -7 * np.abs(xf).sum(axis=0)
     del xs
     ref = None
-    for budget in (0, 4, 8, 16):
+    for variant, budget in (("ldst", 0), ("ldst", 4), ("ldst", 8), ("ldst", 16),
+                            ("tma", 0), ("tma", 4), ("tma", 8), ("tma", 16)):
         outs = RankBuffers(None, n, storage, p=p)
         with Comm(ins, outs) as cm:
-            ccl.ccl_set_launch(cm.h, budget, "ldst", 0)
+            ccl.ccl_set_launch(cm.h, budget, variant, 0)
             ccl.ccl_allreduce(cm.h, "sum", dtype, n, "ring", stream_ptr())
             torch.cuda.synchronize()
             desc = ccl.ccl_comm_last_launch(cm.h)
@@ -422,6 +427,20 @@ def test_moe_p16_sm_budgets():
         else:
             assert torch.equal(outs.views[0], ref), budget
         assert outs.guards_intact()
+        del outs
+        torch.cuda.empty_cache()
+    # the bulk-reduce variant lets the memory system order the adds: within the
+    # reassociation bound at the sampled elements, identical on every rank
+    for budget in (0, 16):
+        outs = RankBuffers(None, n, storage, p=p)
+        with Comm(ins, outs) as cm:
+            ccl.ccl_set_launch(cm.h, budget, "tma_bulkred", 0)
+            ccl.ccl_allreduce(cm.h, "sum", dtype, n, "ring", stream_ptr())
+            torch.cuda.synchronize()
+            ccl.ccl_comm_check(cm.h)
+        got = torch.from_numpy(outs.at(0, idx).view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+        assert np.all(np.abs(got - exact) <= bound), budget
+        assert outs.identical_across_ranks()
         del outs
         torch.cuda.empty_cache()
 
