@@ -436,14 +436,18 @@ def run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes, n):
 
 
 def run_variants(comm, sptr, stream, peak, n, args):
-    """The benchmark AllReduce through each kernel variant (all SMs).  GB/s
-    counts the AllReduce's algorithmic bytes 2*p*n*s for all of them; the
-    bulk-reduce variant moves 2*(p+1)*n*s (ReduceScatter then AllGather)."""
+    """The benchmark AllReduce through each kernel variant and comparison
+    executor (all SMs).  GBps counts the AllReduce's algorithmic bytes 2*p*n*s
+    for all of them; bytes_moved is what each one actually moves: 2(p+1)ns for
+    bulk-reduce (ReduceScatter then AllGather), 5(p-1)ns for the stepwise
+    ring, (p^2+p)ns for one-phase all-pairs."""
     import torch
     import reducescatter_reduction_gb300 as ccl
 
     rows = {}
-    for variant in ("ldst", "tma", "tma_bulkred"):
+    moved = {"ldst": 2 * P, "tma": 2 * P, "tma_bulkred": 2 * (P + 1), "ring_stepwise": 5 * (P - 1),
+             "one_phase": P * P + P}                       # bytes moved per n*s
+    for variant in ("ldst", "tma", "tma_bulkred", "ring_stepwise", "one_phase"):
         ccl.ccl_set_launch(comm, 0, variant, 0)
         for _ in range(3):
             ccl.ccl_allreduce(comm, "sum", "bf16", n, "ring", sptr)
@@ -458,7 +462,9 @@ def run_variants(comm, sptr, stream, peak, n, args):
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / iters
         gbs = 2 * P * n * S / (us * 1e-6) / 1e9
+        moved_gbs = moved[variant] * n * S / (us * 1e-6) / 1e9
         rows[variant] = {"us": round(us, 1), "GBps": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+                         "bytes_moved": moved[variant] * n * S, "moved_GBps": round(moved_gbs, 1),
                          "launch": ccl.ccl_comm_last_launch(comm)}
     ccl.ccl_set_launch(comm, args.sm_budget, args.variant, 0)
     ccl.ccl_comm_check(comm)

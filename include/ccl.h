@@ -107,7 +107,16 @@ typedef enum {
     CCL_VARIANT_AUTO = 0,    /* ld/st with every SM; TMA under an SM budget when the layout allows it */
     CCL_VARIANT_LDST = 1,    /* 128-bit register loads/stores, fixed order */
     CCL_VARIANT_TMA = 2,     /* cp.async.bulk into shared-memory stages, fixed order */
-    CCL_VARIANT_TMA_BULKRED = 3 /* cp.reduce.async.bulk: order left to the memory system */
+    CCL_VARIANT_TMA_BULKRED = 3, /* cp.reduce.async.bulk: order left to the memory system */
+    /* Comparison executors (AllReduce only), for measuring the pages' other
+     * algorithms on one GPU against the fused kernel: */
+    CCL_VARIANT_RING_STEPWISE = 4, /* the ring hop by hop ("Inside NCCL AllReduce", "The ring, exactly as
+                                      the kernel runs it"): 2(p-1) launches, each partial held in the element
+                                      type in a rank buffer between hops (fp16/bf16 round at every hop; fp32
+                                      and int32 give the fused bits); ring schedule only */
+    CCL_VARIANT_ONE_PHASE = 5      /* one-phase all-pairs (MSCCL++ 1PA): every rank's output reduced
+                                      independently from all p inputs (p^2 n s read); the fused bits;
+                                      out of place only */
 } ccl_variant_t;
 
 /* ---------------------------------------------------------------------------

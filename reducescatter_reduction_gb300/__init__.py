@@ -24,7 +24,8 @@ CCL_OK, CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED, CCL_ERR_CUDA, CCL_ERR_TIMEOUT,
 CCL_SUM, CCL_PROD, CCL_MIN, CCL_MAX, CCL_AVG = range(5)
 CCL_F32, CCL_F16, CCL_BF16, CCL_I32 = range(4)
 CCL_SCHED_AUTO, CCL_SCHED_RING, CCL_SCHED_ALLPAIRS, CCL_SCHED_CUSTOM = range(4)
-CCL_VARIANT_AUTO, CCL_VARIANT_LDST, CCL_VARIANT_TMA, CCL_VARIANT_TMA_BULKRED = range(4)
+(CCL_VARIANT_AUTO, CCL_VARIANT_LDST, CCL_VARIANT_TMA, CCL_VARIANT_TMA_BULKRED, CCL_VARIANT_RING_STEPWISE,
+ CCL_VARIANT_ONE_PHASE) = range(6)
 CCL_MAX_RANKS = 64
 
 OPS = {"sum": CCL_SUM, "prod": CCL_PROD, "min": CCL_MIN, "max": CCL_MAX, "avg": CCL_AVG}
@@ -32,7 +33,8 @@ DTYPES = {"f32": CCL_F32, "f16": CCL_F16, "bf16": CCL_BF16, "i32": CCL_I32}
 SCHEDULES = {"auto": CCL_SCHED_AUTO, "ring": CCL_SCHED_RING, "allpairs": CCL_SCHED_ALLPAIRS,
              "custom": CCL_SCHED_CUSTOM}
 VARIANTS = {"auto": CCL_VARIANT_AUTO, "ldst": CCL_VARIANT_LDST, "tma": CCL_VARIANT_TMA,
-            "tma_bulkred": CCL_VARIANT_TMA_BULKRED}
+            "tma_bulkred": CCL_VARIANT_TMA_BULKRED, "ring_stepwise": CCL_VARIANT_RING_STEPWISE,
+            "one_phase": CCL_VARIANT_ONE_PHASE}
 STATUS_NAMES = {CCL_OK: "CCL_OK", CCL_ERR_INVALID_ARG: "CCL_ERR_INVALID_ARG",
                 CCL_ERR_UNSUPPORTED: "CCL_ERR_UNSUPPORTED", CCL_ERR_CUDA: "CCL_ERR_CUDA",
                 CCL_ERR_TIMEOUT: "CCL_ERR_TIMEOUT", CCL_ERR_NOMEM: "CCL_ERR_NOMEM"}

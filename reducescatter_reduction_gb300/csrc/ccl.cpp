@@ -282,7 +282,7 @@ extern "C" ccl_status_t ccl_set_launch(ccl_comm_t c, int sm_budget, int variant,
 {
     if (!c) return fail(CCL_ERR_INVALID_ARG, "comm is NULL");
     if (sm_budget < 0) return fail(CCL_ERR_INVALID_ARG, "sm_budget %d < 0", sm_budget);
-    if (variant < CCL_VARIANT_AUTO || variant > CCL_VARIANT_TMA_BULKRED)
+    if (variant < CCL_VARIANT_AUTO || variant > CCL_VARIANT_ONE_PHASE)
         return fail(CCL_ERR_INVALID_ARG, "unknown variant %d", variant);
     if (pipe_bytes != 0 && (pipe_bytes % 16 || pipe_bytes < 1024 || pipe_bytes > 32768))
         return fail(CCL_ERR_INVALID_ARG, "pipeline_chunk_bytes %zu not a multiple of 16 in [1024, 32768]",
@@ -350,7 +350,7 @@ static const char *kOpName[] = {"sum", "prod", "min", "max", "avg"};
 static const char *kDtypeName[] = {"f32", "f16", "bf16", "i32"};
 static const char *kSchedName[] = {"auto", "ring", "allpairs", "custom"};
 static const char *kCollName[] = {"allreduce", "reduce_scatter", "all_gather"};
-static const char *kVariantName[] = {"auto", "ldst", "tma", "tma_bulkred"};
+static const char *kVariantName[] = {"auto", "ldst", "tma", "tma_bulkred", "ring_stepwise", "one_phase"};
 
 enum Coll { COLL_AR = 0, COLL_RS = 1, COLL_AG = 2 };
 
@@ -428,6 +428,10 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
             if (ok && tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem)) variant = CCL_VARIANT_TMA;
         }
     }
+    if ((variant == CCL_VARIANT_RING_STEPWISE || variant == CCL_VARIANT_ONE_PHASE) && coll != COLL_AR)
+        return fail(CCL_ERR_UNSUPPORTED, "the %s executor is an AllReduce", kVariantName[variant]);
+    if (variant == CCL_VARIANT_RING_STEPWISE && schedule != CCL_SCHED_AUTO && schedule != CCL_SCHED_RING)
+        return fail(CCL_ERR_UNSUPPORTED, "the stepwise ring runs the ring schedule only");
     if ((variant == CCL_VARIANT_TMA || variant == CCL_VARIANT_TMA_BULKRED) && coll == COLL_AG)
         return fail(CCL_ERR_UNSUPPORTED, "AllGather has no TMA variant in this build (use ld/st)");
     if (variant == CCL_VARIANT_TMA_BULKRED && !bulkred_supported(dtype, op))
@@ -440,6 +444,10 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     uint64_t self_mask = 0;
     ccl_status_t st = check_aliases(c, coll, n, s, &self_mask);
     if (st != CCL_OK) return st;
+    if (variant == CCL_VARIANT_ONE_PHASE)
+        for (int r = 0; r < p; ++r)
+            if (c->out[r] == c->in[r])  // rank r's output would overwrite an input other ranks still read
+                return fail(CCL_ERR_UNSUPPORTED, "the one-phase executor needs outputs distinct from the inputs");
 
     DeviceGuard g(c->device);
     if (g.err != cudaSuccess) return cuda_fail(g.err, kCollName[coll]);
@@ -468,8 +476,15 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
 
     int sched = CCL_SCHED_RING;
     if (coll != COLL_AG) {
-        sched = resolve_schedule(c, schedule, double(n) * double(s));
+        sched = variant == CCL_VARIANT_RING_STEPWISE ? int(CCL_SCHED_RING)
+                                                     : resolve_schedule(c, schedule, double(n) * double(s));
         L.table = get_table(c, n, sched);
+    }
+    if (variant == CCL_VARIANT_RING_STEPWISE || variant == CCL_VARIANT_ONE_PHASE) {
+        // 16-byte groups only where no group straddles a chunk boundary
+        bool ok = aligned;
+        for (int k = 0; k <= p && ok; ++k) ok = (L.table->bound[k] * s) % 16 == 0;
+        L.vec = ok;
     }
     if (variant == CCL_VARIANT_TMA || variant == CCL_VARIANT_TMA_BULKRED) {
         // bulk copies move 16-byte multiples between 16-byte aligned addresses
@@ -497,6 +512,16 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
         case CCL_F16: err = launch_tma_f16(L, &info); break;
         case CCL_BF16: err = launch_tma_bf16(L, &info); break;
         default: err = launch_tma_i32(L, &info); break;
+        }
+    } else if ((variant == CCL_VARIANT_RING_STEPWISE && p > 1) || variant == CCL_VARIANT_ONE_PHASE) {
+        err = launch_compare(L, &info, variant == CCL_VARIANT_RING_STEPWISE);
+    } else if (variant == CCL_VARIANT_RING_STEPWISE) {
+        // p = 1: no hop to take; the one contribution is the result
+        switch (dtype) {
+        case CCL_F32: err = launch_reduce_f32(L, &info); break;
+        case CCL_F16: err = launch_reduce_f16(L, &info); break;
+        case CCL_BF16: err = launch_reduce_bf16(L, &info); break;
+        default: err = launch_reduce_i32(L, &info); break;
         }
     } else if (variant == CCL_VARIANT_TMA_BULKRED) {
         switch (dtype) {

@@ -135,6 +135,10 @@ cudaError_t launch_bulkred_i32(const Launch &L, LaunchInfo *info);
 // AllGather (broadcast store), dtype-agnostic beyond the element size.
 cudaError_t launch_gather(const Launch &L, LaunchInfo *info);
 
+// Comparison executors: the ring run hop by hop (stepwise = true) or the
+// one-phase all-pairs reduction (stepwise = false); AllReduce only.
+cudaError_t launch_compare(const Launch &L, LaunchInfo *info, bool stepwise);
+
 // Sets the message ccl_last_error() returns on this host thread; returns st.
 ccl_status_t record_error(ccl_status_t st, const char *msg);
 
