@@ -60,6 +60,8 @@ def lib():
         L.oracle_all_gather.argtypes = [i32, u64, i32, pp, pp]
         L.oracle_allreduce_orders.argtypes = [i32, u64, i32, i32, ctypes.POINTER(ctypes.c_uint8), pp, pp]
         L.oracle_allreduce_ring_stepwise.argtypes = [i32, u64, i32, i32, pp, pp]
+        L.oracle_allreduce_residual_rmsnorm.argtypes = [i32, u64, u64, i32, i32, pp, vp, vp,
+                                                        ctypes.c_double, vp, vp]
         L.oracle_allreduce_at.argtypes = [i32, u64, i32, i32, i32, pp,
                                           ctypes.POINTER(u64), u64, vp]
         L.oracle_chunk_bounds.argtypes = [i32, u64, i32, ctypes.POINTER(u64), ctypes.POINTER(u64)]
@@ -134,6 +136,19 @@ def allreduce_ring_stepwise(xs, op, dtype):
     if lib().oracle_allreduce_ring_stepwise(len(xs), n, dt, o, _ptrs(xs), _ptrs(ys)):
         raise ValueError("oracle_allreduce_ring_stepwise rejected its arguments")
     return ys
+
+
+def allreduce_residual_rmsnorm(xs, residual, gamma, rows, hidden, dtype, schedule="ring", eps=1e-6):
+    """AllReduce (sum) + residual merge + RMSNorm; returns (out, residual_out)."""
+    dt, s = _code(DTYPES, dtype), _code(SCHEDULES, schedule)
+    _check_inputs(list(xs) + [residual, gamma], dt)
+    out = np.empty(rows * hidden, dtype=NP_STORAGE[dt])
+    res_out = np.empty(rows * hidden, dtype=NP_STORAGE[dt])
+    if lib().oracle_allreduce_residual_rmsnorm(len(xs), rows, hidden, dt, s, _ptrs(xs),
+                                               residual.ctypes.data, gamma.ctypes.data, float(eps),
+                                               out.ctypes.data, res_out.ctypes.data):
+        raise ValueError("oracle_allreduce_residual_rmsnorm rejected its arguments")
+    return out, res_out
 
 
 def reduce_scatter(xs, op, dtype, schedule="ring"):

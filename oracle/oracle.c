@@ -321,6 +321,49 @@ int oracle_allreduce_ring_stepwise(int p, uint64_t n, int dtype, int op, const v
     return 0;
 }
 
+/* AllReduce followed by the merge into the residual stream and RMSNorm,
+ * fused in the all-reduce ("Inside NCCL AllReduce", last section: in decoding
+ * "the merge and the RMSNorm that follow are fused into the preceding
+ * all-reduce").  The pages give no formula; the plain reading, per element of
+ * a [rows, hidden] buffer:
+ *   y   = the sum AllReduce of the p inputs (schedule order, fp32, rounded)
+ *   h   = round(fl32(y) + fl32(residual))            -- the merge
+ *   out = round(h / sqrt(mean_row(h^2) + eps) * gamma) -- RMSNorm (Zhang and
+ *         Sennrich, 2019); the norm is computed here in fp64
+ * out goes to every rank; residual_out receives h.  dtype f32/f16/bf16. */
+int oracle_allreduce_residual_rmsnorm(int p, uint64_t rows, uint64_t hidden, int dtype, int schedule,
+                                      const void *const *x, const void *residual, const void *gamma,
+                                      double eps, void *out, void *residual_out)
+{
+    if (dtype == OR_I32 || hidden == 0) return -1;
+    if (check_args(p, dtype, OR_SUM, schedule)) return -1;
+    uint64_t n = rows * hidden;
+    int order[64];
+    for (uint64_t row = 0; row < rows; ++row) {
+        double ss = 0.0;
+        for (uint64_t j = 0; j < hidden; ++j) {
+            uint64_t e = row * hidden + j;
+            uint64_t q = n / (uint64_t)p, r = n % (uint64_t)p;
+            uint64_t c = (e < r * (q + 1)) ? e / (q + 1) : r + (e - r * (q + 1)) / q;
+            oracle_chunk_order(p, schedule, (int)c, order);
+            unsigned char ybuf[4];
+            reduce_element(p, dtype, OR_SUM, order, x, e, ybuf, 0);
+            float h = load_f(dtype, ybuf, 0) + load_f(dtype, residual, e);
+            store_f(dtype, residual_out, e, h);
+            double hv = (double)load_f(dtype, residual_out, e);
+            ss += hv * hv;
+        }
+        double inv = 1.0 / sqrt(ss / (double)hidden + eps);
+        for (uint64_t j = 0; j < hidden; ++j) {
+            uint64_t e = row * hidden + j;
+            double hv = (double)load_f(dtype, residual_out, e);
+            double g = (double)load_f(dtype, gamma, j);
+            store_f(dtype, out, e, (float)(hv * inv * g));
+        }
+    }
+    return 0;
+}
+
 /* ReduceScatter: rank r's output y[r] receives chunk r of the reduction,
  * n/p elements written from offset 0.  Requires n % p == 0. */
 int oracle_reduce_scatter(int p, uint64_t n, int dtype, int op, int schedule,

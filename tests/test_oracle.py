@@ -578,3 +578,85 @@ def test_ring_stepwise_wide_types_match_fused(dtype, op):
     b = oracle.allreduce(xs, op, dtype, "ring")
     for r in range(p):
         assert np.array_equal(a[r].view(np.uint8), b[r].view(np.uint8))
+
+
+# ---------------------------------------------------------------------------
+# AllReduce + residual merge + RMSNorm
+# ---------------------------------------------------------------------------
+
+def _rms_case(p, rows, hidden, dtype, seed, sigma=0.02):
+    xs = [inputs.normal(rows * hidden, seed, r, sigma, dtype) for r in range(p)]
+    res = inputs.normal(rows * hidden, seed, 100, 1.0, dtype)
+    gamma = inputs.normal(hidden, seed, 200, 1.0, dtype)
+    return xs, res, gamma
+
+
+def test_rmsnorm_closed_form_three_four():
+    """A [3, 4] row (after the merge) has RMS 5/sqrt(2): out = [3, 4] * sqrt(2)/5."""
+    xs = [to_storage([1.0, 2.0], "f32"), to_storage([2.0, 2.0], "f32")]   # sum = [3, 4]
+    res = to_storage([0.0, 0.0], "f32")
+    gamma = to_storage([1.0, 1.0], "f32")
+    out, h = oracle.allreduce_residual_rmsnorm(xs, res, gamma, 1, 2, "f32", eps=0.0)
+    assert h.tolist() == [3.0, 4.0]
+    want = np.float32(np.array([3.0, 4.0]) * math.sqrt(2.0) / 5.0)
+    assert np.array_equal(out, want)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_rmsnorm_constant_rows_give_sign_times_gamma(dtype):
+    p, rows, hidden = 4, 3, 64
+    vals = [0.5, -2.0, 1.0]
+    xs = [to_storage(np.repeat([v / p for v in vals], hidden), dtype) for _ in range(p)]
+    res = to_storage(np.zeros(rows * hidden), dtype)
+    gamma = to_storage(np.linspace(-2, 2, hidden), dtype)
+    out, h = oracle.allreduce_residual_rmsnorm(xs, res, gamma, rows, hidden, dtype, eps=0.0)
+    g = as_float(gamma, dtype)
+    o = as_float(out, dtype).reshape(rows, hidden)
+    for i, v in enumerate(vals):
+        assert np.array_equal(o[i], as_float(to_storage(np.sign(v) * g, dtype), dtype))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rmsnorm_invariants(dtype):
+    """Unit gamma and eps = 0: every output row has mean square 1, and scaling
+    the inputs and residual by a power of two leaves the output unchanged."""
+    p, rows, hidden = 8, 4, 256
+    xs, res, _ = _rms_case(p, rows, hidden, dtype, 40)
+    ones = to_storage(np.ones(hidden), dtype)
+    out, h = oracle.allreduce_residual_rmsnorm(xs, res, ones, rows, hidden, dtype, eps=0.0)
+    o = as_float(out, dtype).reshape(rows, hidden)
+    tol = 2e-6 if dtype == "f32" else 2e-2
+    assert np.all(np.abs((o ** 2).mean(axis=1) - 1.0) < tol)
+    xs2 = [to_storage(as_float(x, dtype) * 8.0, dtype) for x in xs]
+    res2 = to_storage(as_float(res, dtype) * 8.0, dtype)
+    out2, h2 = oracle.allreduce_residual_rmsnorm(xs2, res2, ones, rows, hidden, dtype, eps=0.0)
+    assert np.array_equal(out2, out)
+    assert np.array_equal(as_float(h2, dtype), as_float(h, dtype) * 8.0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("sched", ["ring", "allpairs"])
+def test_rmsnorm_merge_is_allreduce_plus_residual(dtype, sched):
+    """h is the sum AllReduce, rounded, plus the residual, rounded once more."""
+    p, rows, hidden = 8, 3, 128
+    xs, res, gamma = _rms_case(p, rows, hidden, dtype, 41, sigma=1.0)
+    _, h = oracle.allreduce_residual_rmsnorm(xs, res, gamma, rows, hidden, dtype, sched)
+    y = as_float(oracle.allreduce(xs, "sum", dtype, sched)[0], dtype)
+    want = to_storage(np.float32(y) + np.float32(as_float(res, dtype)), dtype)
+    assert np.array_equal(h, want)
+
+
+def test_rmsnorm_rejects():
+    xs = [np.zeros(4, dtype=np.int32)] * 2
+    with pytest.raises((ValueError, TypeError)):
+        oracle.allreduce_residual_rmsnorm(xs, xs[0], xs[0][:2], 2, 2, "i32")
+
+
+def test_rmsnorm_closed_form_with_eps():
+    """eps enters under the square root: [3, 4] with eps = 0.5 has mean square
+    12.5, so out = [3, 4] / sqrt(13)."""
+    xs = [to_storage([3.0, 4.0], "f32")]
+    res = to_storage([0.0, 0.0], "f32")
+    gamma = to_storage([1.0, 1.0], "f32")
+    out, _ = oracle.allreduce_residual_rmsnorm(xs, res, gamma, 1, 2, "f32", eps=0.5)
+    assert np.array_equal(out, np.float32(np.array([3.0, 4.0]) / math.sqrt(13.0)))
