@@ -338,6 +338,7 @@ def run_ours(args, dist: Dist):
     if not args.no_budgets:
         torch.cuda.empty_cache()
         result["sm_budgets"] = run_budgets(dev, sptr, stream, peak)
+        result["fused_rmsnorm"] = run_rmsnorm(dev, peak)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline_from(ins)
     del ins
@@ -504,6 +505,82 @@ def run_rs_ag(args, ins, outs, sptr, stream, peak, n):
     ccl.ccl_comm_destroy(rs)
     ccl.ccl_comm_destroy(ag)
     return rows
+
+
+def run_rmsnorm(dev, peak):
+    """AllReduce fused with the residual merge and RMSNorm at TP=8 (p=8 bf16,
+    hidden 8192), decode (1 token) and prefill (4096 tokens), against the
+    AllReduce alone and against the AllReduce followed by the same epilogue in
+    torch on one rank's copy (a lower bound for the unfused path, which would
+    also write p outputs).  Per-call device time from CUDA-graph replay."""
+    import torch
+    import reducescatter_reduction_gb300 as ccl
+
+    p, hidden = 8, 8192
+    rows_out = {}
+    for tokens in (1, 4096):
+        n = tokens * hidden
+        ins = [(0.02 * torch.randn(n, device=dev)).to(torch.bfloat16) for _ in range(p)]
+        outs = [torch.empty_like(t) for t in ins]
+        res = torch.randn(n, device=dev).to(torch.bfloat16)
+        res_out = torch.empty_like(res)
+        gamma = torch.randn(hidden, device=dev).to(torch.bfloat16)
+        h = ccl.ccl_comm_create(p, [t.data_ptr() for t in ins])
+        ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
+
+        def fused(s):
+            ccl.ccl_allreduce_residual_rmsnorm(h, "bf16", tokens, hidden, res.data_ptr(), res_out.data_ptr(),
+                                               gamma.data_ptr(), 1e-6, "ring", s)
+
+        def ar_only(s):
+            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s)
+
+        def unfused(s):
+            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s)
+            y = outs[0].view(tokens, hidden)
+            hh = (y.float() + res.view(tokens, hidden).float()).to(torch.bfloat16)
+            hf = hh.float()
+            o = hf * torch.rsqrt(hf.pow(2).mean(-1, keepdim=True) + 1e-6) * gamma.float()
+            res_out.view(tokens, hidden).copy_(hh)
+            outs[1].view(tokens, hidden).copy_(o.to(torch.bfloat16))
+
+        calls = 50 if tokens == 1 else 10
+        row = {}
+        fused(torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        fused_launch = ccl.ccl_comm_last_launch(h)
+        for name, fn in (("fused", fused), ("allreduce_only", ar_only), ("allreduce_then_torch_epilogue", unfused)):
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                fn(side.cuda_stream)                      # warm-up (kernel attributes, torch caches)
+                side.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    cs = torch.cuda.current_stream().cuda_stream
+                    for _ in range(calls):
+                        fn(cs)
+            torch.cuda.current_stream().wait_stream(side)
+            g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(5):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            row[name] = {"us": round(e0.elapsed_time(e1) * 1e3 / (5 * calls), 2)}
+        nbytes = (2 * p + 2) * n * S + hidden * S
+        row["fused"]["bytes"] = nbytes
+        row["fused"]["GBps"] = round(nbytes / (row["fused"]["us"] * 1e-6) / 1e9, 1)
+        row["fused"]["frac_of_hbm_peak"] = round(row["fused"]["GBps"] / peak, 4)
+        row["launch"] = fused_launch
+        rows_out[f"tokens_{tokens}"] = row
+        ccl.ccl_comm_destroy(h)
+        del ins, outs, res, res_out
+        torch.cuda.empty_cache()
+    return rows_out
 
 
 def run_budgets(dev, sptr, stream, peak):

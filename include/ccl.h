@@ -211,6 +211,28 @@ CCL_API ccl_status_t ccl_reduce_scatter(ccl_comm_t comm, ccl_op_t op, ccl_dtype_
  * Bytes moved: n*s read + p*n*s written (in place: (p-1)*n*s written). */
 CCL_API ccl_status_t ccl_all_gather(ccl_comm_t comm, ccl_dtype_t dtype, size_t n, void *stream);
 
+/* AllReduce fused with the residual merge and RMSNorm, for a tensor-parallel
+ * decode step ("Inside NCCL AllReduce", last section: "the merge and the
+ * RMSNorm that follow are fused into the preceding all-reduce").  The
+ * communicator's p input buffers are [rows, hidden] row-major (n = rows*hidden
+ * elements each).  Per element:
+ *   y   = the sum AllReduce of the p inputs, in the schedule's order (fp32,
+ *         rounded to dtype) -- exactly ccl_allreduce's result;
+ *   h   = round(y + residual_in)       -> residual_out (one buffer)
+ *   out = round(h * (1/sqrt(mean_row(h^2) + eps)) * gamma[col]) -> every
+ *         rank's output buffer.
+ * dtype f32, f16 or bf16 (int32: CCL_ERR_UNSUPPORTED).  residual_in /
+ * residual_out: device buffers of n elements; residual_out may equal
+ * residual_in (in place) and must otherwise overlap nothing.  gamma: device
+ * buffer of hidden elements.  Neither residual_in nor gamma may overlap an
+ * output.  Rank buffers follow ccl_allreduce's aliasing rules.  The rounding
+ * of y and h is exact; the row's mean square is summed in fp32 in a tree, so
+ * out may differ from a fp64 evaluation by one unit in the last place of
+ * dtype.  Bytes moved: (2p + 2) n s + hidden s. */
+CCL_API ccl_status_t ccl_allreduce_residual_rmsnorm(ccl_comm_t comm, ccl_dtype_t dtype, size_t rows, size_t hidden,
+                                                    const void *residual_in, void *residual_out, const void *gamma,
+                                                    float eps, ccl_schedule_t schedule, void *stream);
+
 /* AllReduce for callers that cannot allocate device memory.  The pages have
  * no counterpart: this entry point exists for code that may not call
  * cudaMalloc -- a plug-in inside an application that owns all device memory

@@ -575,3 +575,79 @@ extern "C" ccl_status_t ccl_all_gather(ccl_comm_t c, ccl_dtype_t dtype, size_t n
 {
     return run(c, COLL_AG, CCL_SUM, dtype, n, CCL_SCHED_RING, stream);
 }
+
+extern "C" ccl_status_t ccl_allreduce_residual_rmsnorm(ccl_comm_t c, ccl_dtype_t dtype, size_t rows, size_t hidden,
+                                                       const void *residual_in, void *residual_out, const void *gamma,
+                                                       float eps, ccl_schedule_t schedule, void *stream)
+{
+    if (!c) return fail(CCL_ERR_INVALID_ARG, "comm is NULL");
+    if (dtype == CCL_I32) return fail(CCL_ERR_UNSUPPORTED, "RMSNorm needs a floating-point dtype");
+    if (dtype < CCL_F32 || dtype > CCL_BF16) return fail(CCL_ERR_INVALID_ARG, "unknown dtype %d", int(dtype));
+    if (schedule < CCL_SCHED_AUTO || schedule > CCL_SCHED_CUSTOM)
+        return fail(CCL_ERR_INVALID_ARG, "unknown schedule %d", int(schedule));
+    if (schedule == CCL_SCHED_CUSTOM && !c->has_custom)
+        return fail(CCL_ERR_INVALID_ARG, "custom schedule requested but none set");
+    if (hidden == 0) return fail(CCL_ERR_INVALID_ARG, "hidden must be positive");
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return fail(CCL_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    const size_t s = elem_bytes(dtype);
+    if (rows > (SIZE_MAX / 4) / hidden / s) return fail(CCL_ERR_INVALID_ARG, "rows * hidden too large");
+    const size_t n = rows * hidden;
+    if (n == 0) return CCL_OK;
+    if (!residual_in || !residual_out || !gamma) return fail(CCL_ERR_INVALID_ARG, "NULL residual or gamma");
+    const int p = c->p;
+
+    uint64_t self_mask = 0;
+    ccl_status_t st = check_aliases(c, COLL_AR, n, s, &self_mask);
+    if (st != CCL_OK) return st;
+    const Range ri = {uintptr_t(residual_in), uintptr_t(residual_in) + n * s};
+    const Range ro = {uintptr_t(residual_out), uintptr_t(residual_out) + n * s};
+    const Range gm = {uintptr_t(gamma), uintptr_t(gamma) + hidden * s};
+    if (ro.lo != ri.lo && overlap(ro, ri)) return fail(CCL_ERR_INVALID_ARG, "residual_out partly overlaps residual_in");
+    if (overlap(ro, gm)) return fail(CCL_ERR_INVALID_ARG, "gamma overlaps residual_out");
+    for (int r = 0; r < p; ++r) {
+        const Range in = {uintptr_t(c->in[r]), uintptr_t(c->in[r]) + n * s};
+        const Range out = {uintptr_t(c->out[r]), uintptr_t(c->out[r]) + n * s};
+        if (overlap(ro, in) || overlap(ro, out)) return fail(CCL_ERR_INVALID_ARG, "residual_out overlaps rank %d", r);
+        if (overlap(ri, out) || overlap(gm, out))
+            return fail(CCL_ERR_INVALID_ARG, "the output of rank %d overlaps the residual or gamma", r);
+    }
+
+    DeviceGuard g(c->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "allreduce_residual_rmsnorm");
+    Launch L;
+    L.p = p;
+    L.op = CCL_SUM;
+    L.dtype = dtype;
+    L.mode = MODE_AR;
+    L.n = n;
+    const size_t vec_elems = 16 / s;
+    bool aligned = uintptr_t(residual_in) % 16 == 0 && uintptr_t(residual_out) % 16 == 0 &&
+                   uintptr_t(gamma) % 16 == 0 && hidden % vec_elems == 0;
+    for (int r = 0; r < p; ++r) {
+        L.src[r] = c->in[r];
+        L.dst[r] = c->out[r];
+        aligned = aligned && uintptr_t(c->in[r]) % 16 == 0 && uintptr_t(c->out[r]) % 16 == 0;
+    }
+    L.num_sms = c->num_sms;
+    L.stream = static_cast<cudaStream_t>(stream);
+    const int sched = resolve_schedule(c, schedule, double(n) * double(s));
+    L.table = get_table(c, n, sched);
+    for (int k = 0; k <= p && aligned; ++k) aligned = L.table->bound[k] % vec_elems == 0;
+    L.vec = aligned;
+    NormLaunch N;
+    N.residual = residual_in;
+    N.residual_out = residual_out;
+    N.gamma = gamma;
+    N.rows = rows;
+    N.hidden = hidden;
+    N.eps = eps;
+    LaunchInfo info;
+    cudaError_t err = launch_allreduce_rmsnorm(L, N, &info);
+    c->launches += uint64_t(info.kernels);
+    snprintf(c->last, sizeof c->last,
+             "%s dtype=%s op=sum p=%d n=%zu rows=%zu hidden=%zu schedule=%s vec=%d grid=%d block=%d", info.kernel,
+             kDtypeName[dtype], p, n, rows, hidden, kSchedName[sched], L.vec ? 1 : 0, info.grid, info.block);
+    if (debug_on()) fprintf(stderr, "[ccl] %s\n", c->last);
+    if (err != cudaSuccess) return cuda_fail(err, "allreduce_residual_rmsnorm");
+    return CCL_OK;
+}

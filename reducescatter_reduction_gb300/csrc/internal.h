@@ -139,6 +139,17 @@ cudaError_t launch_gather(const Launch &L, LaunchInfo *info);
 // one-phase all-pairs reduction (stepwise = false); AllReduce only.
 cudaError_t launch_compare(const Launch &L, LaunchInfo *info, bool stepwise);
 
+// AllReduce fused with the residual merge and RMSNorm (rmsnorm.cu).
+struct NormLaunch {
+    const void *residual = nullptr;
+    void *residual_out = nullptr;
+    const void *gamma = nullptr;
+    uint64_t rows = 0;
+    uint64_t hidden = 0;
+    float eps = 0.0f;
+};
+cudaError_t launch_allreduce_rmsnorm(const Launch &L, const NormLaunch &N, LaunchInfo *info);
+
 // Sets the message ccl_last_error() returns on this host thread; returns st.
 ccl_status_t record_error(ccl_status_t st, const char *msg);
 

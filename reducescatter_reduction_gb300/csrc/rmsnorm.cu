@@ -1,0 +1,264 @@
+// AllReduce fused with the residual merge and RMSNorm.
+//
+// "Inside NCCL AllReduce", last section: in Kimi's decoding path "the merge
+// and the RMSNorm that follow are fused into the preceding all-reduce", so
+// the collective absorbs a kernel.  Per row of a [rows, hidden] buffer:
+//   y   = sum AllReduce of the p rank rows (schedule order, fp32, rounded)
+//   h   = round(y + residual)                     written to residual_out
+//   out = round(h * (1 / sqrt(mean(h^2) + eps)) * gamma)   written to every rank
+// A thread-block cluster of C CTAs per row, each CTA a slice of the columns
+// (for decode, C up to 8 so that a row of 8192 columns is spread over 1024
+// threads; for many rows, one 512-thread CTA per row).  Pass 1 folds the p inputs, merges the residual, stores h and
+// accumulates the slice's sum of squares of the rounded h; the C partial sums
+// are combined through distributed shared memory (every CTA adds the same C
+// values in the same order, so all slices use one bit-identical 1/rms), and
+// pass 2 re-reads the h values the same thread stored and writes the
+// normalised slice to all p outputs.  Cluster barriers are hardware barriers
+// over co-scheduled CTAs: nothing spins.  Each element
+// is read from the rank inputs once; all arithmetic is fp32 with explicit
+// round-to-nearest operations (1/sqrtf is IEEE-rounded under the default
+// flags).  Bytes: (2p + 2) n s + hidden s.
+#include <cooperative_groups.h>
+
+#include "device.cuh"
+
+namespace ccl {
+
+namespace cg = cooperative_groups;
+
+constexpr int kNormMaxThreads = 512;
+constexpr int kNormMaxCluster = 8;
+
+template <int PM>
+struct NormArgs {
+    const void *src[PM];
+    void *dst[PM];
+    uint64_t bound[PM + 1];
+    uint8_t order[PM][PM];
+    const void *residual;
+    void *residual_out;
+    const void *gamma;
+    uint64_t rows;
+    uint64_t hidden;
+    int p;
+    int vec;        // 16-byte groups: pointers aligned, hidden and every chunk boundary multiples of VEC
+    float eps;
+};
+
+template <typename T, int PM>
+__device__ __forceinline__ float fold_one(const NormArgs<PM> &a, int p, uint64_t e)
+{
+    using Tr = Traits<T>;
+    using F = Fold<T, OP_SUM>;
+    int c = 0;
+    while (e >= a.bound[c + 1]) ++c;
+    float acc = Tr::load1(a.src[a.order[c][0]], e);
+    for (int k = 1; k < p; ++k) acc = F::fold(acc, Tr::load1(a.src[a.order[c][k]], e), 1.0f);
+    return acc;
+}
+
+template <typename T>
+__device__ __forceinline__ float round_to(float v)
+{
+    alignas(4) unsigned char tmp[4];
+    Traits<T>::store1(tmp, 0, v);
+    return Traits<T>::load1(tmp, 0);
+}
+
+__device__ __forceinline__ float block_sum(float v, float *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = lane < int(blockDim.x / 32) ? red[lane] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    v = red[0];
+    __syncthreads();
+    return v;
+}
+
+template <typename T, int P, int THREADS>
+__global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_constant__ NormArgs<(P > 0 ? P : kMaxRanks)> a)
+{
+    using Tr = Traits<T>;
+    using F = Fold<T, OP_SUM>;
+    constexpr int VEC = Tr::VEC;
+    constexpr int S = (VEC == 8) ? 2 : 4;
+    __shared__ float red[32];
+    __shared__ float slice_sum;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = int(cluster.num_blocks());
+    const int q = int(cluster.block_rank());
+    const int p = P > 0 ? P : a.p;
+    const uint64_t H = a.hidden;
+    const uint64_t row = blockIdx.x / C;
+    const uint64_t base = row * H;
+    // this CTA's slice: units are 16-byte groups (vec) or elements
+    const uint64_t units = a.vec ? H / VEC : H;
+    const uint64_t u0 = units * q / C, u1 = units * (q + 1) / C;
+
+    float ss = 0.0f;
+    // pass 1: fold, merge, keep h, sum of squares
+    if (a.vec) {
+        for (uint64_t g = u0 + threadIdx.x; g < u1; g += blockDim.x) {
+            const uint64_t e = base + g * VEC;
+            int c = 0;
+            while (e >= a.bound[c + 1]) ++c;
+            float acc[VEC], v[VEC];
+            if constexpr (P > 0) {
+                uint4 r[P];
+#pragma unroll
+                for (int k = 0; k < P; ++k)
+                    r[k] = ld_stream_v4(static_cast<const char *>(a.src[a.order[c][k]]) + e * S);
+                Tr::unpack(r[0], acc);
+#pragma unroll
+                for (int k = 1; k < P; ++k) {
+                    Tr::unpack(r[k], v);
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) acc[i] = F::fold(acc[i], v[i], 1.0f);
+                }
+            } else {
+                Tr::unpack(ld_stream_v4(static_cast<const char *>(a.src[a.order[c][0]]) + e * S), acc);
+                for (int k = 1; k < p; ++k) {
+                    Tr::unpack(ld_stream_v4(static_cast<const char *>(a.src[a.order[c][k]]) + e * S), v);
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) acc[i] = F::fold(acc[i], v[i], 1.0f);
+                }
+            }
+            Tr::unpack(Tr::pack(acc), acc);                                  // y, rounded
+            Tr::unpack(ld_stream_v4(static_cast<const char *>(a.residual) + e * S), v);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) acc[i] = __fadd_rn(acc[i], v[i]);   // the merge
+            const uint4 hq = Tr::pack(acc);
+            st_v4(static_cast<char *>(a.residual_out) + e * S, hq);
+            Tr::unpack(hq, acc);                                             // h, rounded
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) ss = __fadd_rn(ss, __fmul_rn(acc[i], acc[i]));
+        }
+    } else {
+        for (uint64_t j = u0 + threadIdx.x; j < u1; j += blockDim.x) {
+            const uint64_t e = base + j;
+            const float y = round_to<T>(fold_one<T>(a, p, e));
+            const float h = round_to<T>(__fadd_rn(y, Tr::load1(a.residual, e)));
+            Tr::store1(a.residual_out, e, h);
+            ss = __fadd_rn(ss, __fmul_rn(h, h));
+        }
+    }
+    const float part = block_sum(ss, red);
+    float total = part;
+    if (C > 1) {
+        if (threadIdx.x == 0) slice_sum = part;
+        cluster.sync();                                // every slice's sum is in place
+        total = 0.0f;
+        for (int k = 0; k < C; ++k) total = __fadd_rn(total, *cluster.map_shared_rank(&slice_sum, k));
+        cluster.sync();                                // no CTA leaves while its sum may be read
+    }
+    const float inv = 1.0f / sqrtf(__fadd_rn(__fdiv_rn(total, float(H)), a.eps));
+
+    // pass 2: normalise the h this thread stored, broadcast to every rank
+    if (a.vec) {
+        for (uint64_t g = u0 + threadIdx.x; g < u1; g += blockDim.x) {
+            const uint64_t e = base + g * VEC;
+            float h[VEC], gm[VEC];
+            Tr::unpack(*reinterpret_cast<const uint4 *>(static_cast<const char *>(a.residual_out) + e * S), h);
+            Tr::unpack(*reinterpret_cast<const uint4 *>(static_cast<const char *>(a.gamma) + g * VEC * S), gm);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) h[i] = __fmul_rn(__fmul_rn(h[i], inv), gm[i]);
+            const uint4 out = Tr::pack(h);
+            if constexpr (P > 0) {
+#pragma unroll
+                for (int k = 0; k < P; ++k) st_stream_v4(static_cast<char *>(a.dst[k]) + e * S, out);
+            } else {
+                for (int k = 0; k < p; ++k) st_stream_v4(static_cast<char *>(a.dst[k]) + e * S, out);
+            }
+        }
+    } else {
+        for (uint64_t j = u0 + threadIdx.x; j < u1; j += blockDim.x) {
+            const uint64_t e = base + j;
+            const float o = __fmul_rn(__fmul_rn(Tr::load1(a.residual_out, e), inv), Tr::load1(a.gamma, j));
+            for (int k = 0; k < p; ++k) Tr::store1(a.dst[k], e, o);
+        }
+    }
+}
+
+template <typename T, int P>
+static cudaError_t norm_launch(const Launch &L, const NormLaunch &N, LaunchInfo *info)
+{
+    constexpr int PM = P > 0 ? P : kMaxRanks;
+    NormArgs<PM> a;
+    for (int k = 0; k < L.p; ++k) {
+        a.src[k] = L.src[k];
+        a.dst[k] = L.dst[k];
+    }
+    for (int c = 0; c <= L.p; ++c) a.bound[c] = L.table->bound[c];
+    for (int c = 0; c < L.p; ++c)
+        for (int k = 0; k < L.p; ++k) a.order[c][k] = L.table->order[c * L.p + k];
+    a.residual = N.residual;
+    a.residual_out = N.residual_out;
+    a.gamma = N.gamma;
+    a.rows = N.rows;
+    a.hidden = N.hidden;
+    a.p = L.p;
+    a.vec = L.vec ? 1 : 0;
+    a.eps = N.eps;
+    // Fewer rows than SMs (decode): latency rules, so 128-thread CTAs in a
+    // cluster of up to 8 per row, one unit per thread.  Many rows (prefill):
+    // bytes rule, so 512-thread CTAs, about two units per thread, a cluster
+    // only when a row needs more than one CTA.
+    const uint64_t units = L.vec ? N.hidden / Traits<T>::VEC : N.hidden;
+    const bool few_rows = N.rows < uint64_t(L.num_sms);
+    const int threads = few_rows ? 128 : kNormMaxThreads;
+    const uint64_t per_cta = uint64_t(threads) * (few_rows ? 1 : 2);
+    const uint64_t want = (units + per_cta - 1) / per_cta;
+    const int C = int(want < 1 ? 1 : want > uint64_t(kNormMaxCluster) ? kNormMaxCluster : want);
+    if (N.rows * uint64_t(C) > 0x7fffffffull) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(N.rows * C));
+    cfg.blockDim = dim3(unsigned(threads));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = C > 1 ? 1 : 0;  // one CTA per row: no cluster needed
+    cudaError_t err = few_rows ? cudaLaunchKernelEx(&cfg, ar_rmsnorm_kernel<T, P, 128>, a)
+                               : cudaLaunchKernelEx(&cfg, ar_rmsnorm_kernel<T, P, kNormMaxThreads>, a);
+    if (err != cudaSuccess) return err;
+    const int grid = int(N.rows * C);
+    if (info) {
+        info->kernel = "allreduce_residual_rmsnorm";
+        info->grid = grid;
+        info->block = threads;
+        info->smem = 0;
+        info->kernels = 1;
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t norm_dtype(const Launch &L, const NormLaunch &N, LaunchInfo *info)
+{
+    return L.p == 8 ? norm_launch<T, 8>(L, N, info) : norm_launch<T, 0>(L, N, info);
+}
+
+cudaError_t launch_allreduce_rmsnorm(const Launch &L, const NormLaunch &N, LaunchInfo *info)
+{
+    switch (L.dtype) {
+    case DT_F32: return norm_dtype<F32>(L, N, info);
+    case DT_F16: return norm_dtype<F16>(L, N, info);
+    case DT_BF16: return norm_dtype<BF16>(L, N, info);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace ccl
