@@ -495,3 +495,55 @@ def test_auto_variant_follows_sm_budget():
     xs = gen("bf16", "sum", 4, 4 * 1001, seed=53)       # chunks off the 16-byte grid: ld/st
     _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
     assert "variant=ldst" in desc
+
+
+def test_largest_buffers_64bit_indexing():
+    """n = 2^31 + 64 bf16 per rank (4 GiB buffers, p=2): element indices pass
+    2^31 and byte offsets pass 2^32.  ld/st, TMA and the allocation-free entry
+    point agree with the oracle at sampled elements on both sides of 2^31 and
+    of the chunk boundary n/2.  (With p=2 a sum is one fp32 addition, which is
+    commutative, so the oracle on the sampled values alone is the reference.)"""
+    p, n, dtype = 2, (1 << 31) + 64, "bf16"
+    rng = np.random.default_rng(77)
+    idx = np.unique(np.concatenate([rng.integers(0, n, 20000, dtype=np.int64),
+                                    np.arange((1 << 31) - 64, n, dtype=np.int64),
+                                    np.arange(0, 64, dtype=np.int64),
+                                    np.arange(n // 2 - 16, n // 2 + 16, dtype=np.int64)]))
+    didx = torch.from_numpy(idx).cuda()
+    # seeded values at the sampled places, a constant elsewhere (cheap to build)
+    bufs, xs_at = [], []
+    for r in range(p):
+        t = torch.full((n,), 0x3f80 + r, dtype=torch.int16, device="cuda")
+        vals = inputs.normal(idx.size, 78, r, 1.0, dtype)
+        t[didx] = torch.from_numpy(vals.view(np.int16)).cuda()
+        bufs.append(t)
+        xs_at.append(vals)
+    want = oracle.allreduce(xs_at, "sum", dtype, "ring")[0]
+    for variant in ("ldst", "tma"):
+        out = [torch.empty_like(b) for b in bufs]
+        h = ccl.ccl_comm_create(p, [b.data_ptr() for b in bufs])
+        try:
+            ccl.ccl_comm_set_outputs(h, [o.data_ptr() for o in out])
+            ccl.ccl_set_launch(h, 0, variant, 0)
+            ccl.ccl_allreduce(h, "sum", dtype, n, "ring", stream_ptr())
+            torch.cuda.synchronize()
+            ccl.ccl_comm_check(h)
+        finally:
+            ccl.ccl_comm_destroy(h)
+        for r in range(p):
+            got = out[r][didx].cpu().numpy().view(np.uint16)
+            assert bits_equal(got, want), (variant, r)
+        # an element outside the sample: 1.0 + 1.0078125 = 2.0078125, a bf16 tie -> 2.0 (0x4000)
+        e_const = 1_000_000_007
+        assert not np.isin(e_const, idx)
+        for r in range(p):
+            assert int(out[r][e_const].item()) == 0x4000
+        del out
+        torch.cuda.empty_cache()
+    ccl.ccl_allreduce_static(p, [b.data_ptr() for b in bufs], [b.data_ptr() for b in bufs], "sum", dtype, n,
+                             "ring", stream_ptr())
+    torch.cuda.synchronize()
+    for r in range(p):
+        assert bits_equal(bufs[r][didx].cpu().numpy().view(np.uint16), want)
+    del bufs
+    torch.cuda.empty_cache()
