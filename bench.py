@@ -65,6 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-budgets", action="store_true")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="fit t = alpha + bytes/B per variant and SM budget (p=8 bf16) and print the table")
     ap.add_argument("--n", type=int, default=N,
                     help="bf16 elements per rank (default 2^27; smaller only for profiling runs)")
     return ap.parse_args(argv)
@@ -507,6 +509,64 @@ def run_rs_ag(args, ins, outs, sptr, stream, peak, n):
     return rows
 
 
+def calibrate(dev):
+    """Per-call device time of the p=8 bf16 AllReduce for the ld/st and TMA
+    variants at several SM budgets over 16 KiB .. 256 MiB per rank (CUDA-graph
+    replay below 8 MiB, events above), and a least-squares fit of
+    t = alpha + bytes / B (bytes = 2 p n s) on relative error."""
+    import numpy as np
+    import torch
+    import reducescatter_reduction_gb300 as ccl
+
+    sizes = [1 << k for k in range(13, 28, 2)]              # bf16 elements per rank
+    big = [(torch.randn(sizes[-1], device=dev)).to(torch.bfloat16) for _ in range(P)]
+    outs = [torch.empty_like(t) for t in big]
+    table = []
+    for variant in ("ldst", "tma"):
+        for budget in (0, 8, 16, 32, 76):
+            ts = []
+            for n in sizes:
+                h = ccl.ccl_comm_create(P, [t.data_ptr() for t in big])
+                ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
+                ccl.ccl_set_launch(h, budget, variant, 0)
+                s = torch.cuda.current_stream()
+                ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s.cuda_stream)
+                torch.cuda.synchronize()
+                calls = 100 if n * S * P < (64 << 20) else 5
+                side = torch.cuda.Stream()
+                side.wait_stream(s)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(side):
+                    with torch.cuda.graph(g, stream=side):
+                        cs = torch.cuda.current_stream().cuda_stream
+                        for _ in range(calls):
+                            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", cs)
+                s.wait_stream(side)
+                g.replay()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(3):
+                    g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e-3 / (3 * calls))
+                ccl.ccl_comm_destroy(h)
+            x = np.array([2.0 * P * n * S for n in sizes])
+            t = np.array(ts)
+            # minimise sum ((alpha + x/B - t) / t)^2: linear in (alpha, 1/B)
+            A = np.stack([1.0 / t, x / t], axis=1)
+            coef, *_ = np.linalg.lstsq(A, np.ones_like(t), rcond=None)
+            alpha, inv_b = float(coef[0]), float(coef[1])
+            pred = alpha + x * inv_b
+            table.append({"variant": variant, "sm_budget": budget, "alpha_us": round(alpha * 1e6, 3),
+                          "B_GBps": round(1.0 / inv_b / 1e9, 1),
+                          "max_rel_residual": round(float(np.max(np.abs(pred - t) / t)), 3),
+                          "points_us": [round(v * 1e6, 2) for v in ts]})
+    return {"sizes_bytes_per_rank": [n * S for n in sizes], "fits": table}
+
+
 def run_rmsnorm(dev, peak):
     """AllReduce fused with the residual merge and RMSNorm at TP=8 (p=8 bf16,
     hidden 8192), decode (1 token) and prefill (4096 tokens), against the
@@ -789,6 +849,12 @@ def run_reference(args, dist: Dist):
 def main(argv=None):
     args = parse_args(argv)
     dist = Dist()
+    if args.calibrate:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        print(json.dumps(calibrate(torch.device("cuda", dist.local_rank))), flush=True)
+        return 0
     if args.impl == "reference":
         res = run_reference(args, dist)
     else:

@@ -104,7 +104,8 @@ typedef enum {
 } ccl_schedule_t;
 
 typedef enum {
-    CCL_VARIANT_AUTO = 0,    /* ld/st with every SM; TMA under an SM budget when the layout allows it */
+    CCL_VARIANT_AUTO = 0,    /* ld/st with every SM; under an SM budget, TMA from a measured per-budget
+                                message size on (256 KiB .. 2 MiB per rank) when the layout allows it */
     CCL_VARIANT_LDST = 1,    /* 128-bit register loads/stores, fixed order */
     CCL_VARIANT_TMA = 2,     /* cp.async.bulk into shared-memory stages, fixed order */
     CCL_VARIANT_TMA_BULKRED = 3, /* cp.reduce.async.bulk: order left to the memory system */

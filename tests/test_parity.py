@@ -486,12 +486,17 @@ def test_cuda_graph_capture_and_replay(variant):
 
 
 def test_auto_variant_follows_sm_budget():
-    p, n = 16, 16 * 65536
+    """AUTO follows the measured launch table: ld/st with every SM; under a
+    16-SM budget, ld/st below 1 MiB per rank and TMA from there on."""
+    p, n = 16, 16 * 65536                                 # 2 MiB per rank
     xs = gen("bf16", "sum", p, n, seed=52)
     _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto")
     assert "variant=ldst" in desc
     _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
     assert "variant=tma" in desc and "grid=16" in desc
+    small = gen("bf16", "sum", p, 16 * 8192, seed=54)     # 256 KiB per rank
+    _, desc = run_collective(small, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
+    assert "variant=ldst" in desc and "grid=16" in desc
     xs = gen("bf16", "sum", 4, 4 * 1001, seed=53)       # chunks off the 16-byte grid: ld/st
     _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
     assert "variant=ldst" in desc
