@@ -38,10 +38,12 @@
  * contribution is multiplied by fl32(1/p) as it is read, and an int32 avg is
  * the wrapped int32 sum divided by p with truncation toward zero ("Inside
  * NCCL AllReduce", "What all-reduce promises").  int32 sum/prod wrap modulo
- * 2^32.  The ld/st and TMA copy variants keep this order exactly; the TMA
- * bulk-reduce variant (CCL_VARIANT_TMA_BULKRED) lets the memory system apply
- * the adds and is held to |err| <= 2 * p * eps(element type) * sum_k |x_k|
- * per element instead.
+ * 2^32.  The ld/st and TMA copy variants and the one-phase executor keep this
+ * order exactly (identical bits); the TMA bulk-reduce variant
+ * (CCL_VARIANT_TMA_BULKRED) lets the memory system apply the adds and is held
+ * to |err| <= 2 * p * eps(element type) * sum_k |x_k| per element instead; the
+ * stepwise-ring executor rounds each partial to the element type at every hop
+ * (see ccl_variant_t).
  *
  * Memory and ownership.  The caller allocates and owns every rank buffer
  * (device memory, e.g. from PyTorch).  A communicator copies the p input and
@@ -53,7 +55,10 @@
  * enqueue kernels on `stream` (a cudaStream_t passed as void*, NULL = the
  * legacy default stream) and return without synchronising.  Errors detected
  * on the host are returned at once; a bounded device-side wait that gave up
- * is reported by ccl_comm_check().
+ * is reported by ccl_comm_check().  Because they only enqueue, the
+ * communicator collectives can be captured in a CUDA graph, provided each
+ * variant and SM budget has run once on the device before capture (the first
+ * launch sets kernel attributes).
  *
  * Alignment.  All pointers 16-byte aligned (and, for ReduceScatter /
  * AllGather, (n/p) * element size a multiple of 16) take the 128-bit vector
@@ -152,11 +157,16 @@ CCL_API ccl_status_t ccl_comm_set_schedule(ccl_comm_t comm, const uint8_t *order
 /* Launch shape.
  *  sm_budget : 0 = all SMs; k > 0 = at most k CTAs, one per SM (persistent),
  *              the restricted-CTA-budget setting of T-CCL, section
- *              "Collective Operation Performance" (Fig. 4, Table IV).  Larger than the SM count = all SMs.
+ *              "Collective Operation Performance" (Fig. 4, Table IV).  Larger
+ *              than the SM count = all SMs.  The comparison executors and
+ *              ccl_allreduce_residual_rmsnorm always use every SM.
  *  variant   : a ccl_variant_t.
  *  pipeline_chunk_bytes : 0 = the variant's default.  For the TMA variants,
  *              the bytes per rank moved per pipeline stage (multiple of 16,
- *              1 KiB .. 32 KiB).  Results never depend on it.
+ *              1 KiB .. 32 KiB); a size whose stages do not fit in shared
+ *              memory for the communicator's p is refused at the collective
+ *              call (CCL_ERR_INVALID_ARG).  Results of the fixed-order variants
+ *              never depend on it.
  * Errors: CCL_ERR_INVALID_ARG for a negative budget, an unknown variant or a
  * chunk size outside the range. */
 CCL_API ccl_status_t ccl_set_launch(ccl_comm_t comm, int sm_budget, int variant,
