@@ -65,6 +65,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-budgets", action="store_true")
+    ap.add_argument("--rmsnorm-tokens", type=int, default=0,
+                    help="profiling mode: only the fused AllReduce + residual + RMSNorm, p=8 bf16, "
+                         "[tokens, 8192], warmup + steps calls")
     ap.add_argument("--calibrate", action="store_true",
                     help="fit t = alpha + bytes/B per variant and SM budget (p=8 bf16) and print the table")
     ap.add_argument("--n", type=int, default=N,
@@ -849,6 +852,37 @@ def run_reference(args, dist: Dist):
 def main(argv=None):
     args = parse_args(argv)
     dist = Dist()
+    if args.rmsnorm_tokens:
+        import torch
+        import __graft_entry__
+        import reducescatter_reduction_gb300 as ccl
+        __graft_entry__.build()
+        dev = torch.device("cuda", dist.local_rank)
+        tokens, hidden, n = args.rmsnorm_tokens, 8192, args.rmsnorm_tokens * 8192
+        ins = [(0.02 * torch.randn(n, device=dev)).to(torch.bfloat16) for _ in range(P)]
+        outs = [torch.empty_like(t) for t in ins]
+        res = torch.randn(n, device=dev).to(torch.bfloat16)
+        res_out = torch.empty_like(res)
+        gamma = torch.randn(hidden, device=dev).to(torch.bfloat16)
+        h = ccl.ccl_comm_create(P, [t.data_ptr() for t in ins])
+        ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
+        s = torch.cuda.current_stream()
+        for _ in range(args.warmup):
+            ccl.ccl_allreduce_residual_rmsnorm(h, "bf16", tokens, hidden, res.data_ptr(), res_out.data_ptr(),
+                                               gamma.data_ptr(), 1e-6, "ring", s.cuda_stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            ccl.ccl_allreduce_residual_rmsnorm(h, "bf16", tokens, hidden, res.data_ptr(), res_out.data_ptr(),
+                                               gamma.data_ptr(), 1e-6, "ring", s.cuda_stream)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / max(1, args.steps)
+        print(json.dumps({"mode": "rmsnorm", "tokens": tokens, "us_per_call": round(us, 2),
+                          "launch": ccl.ccl_comm_last_launch(h)}), flush=True)
+        ccl.ccl_comm_destroy(h)
+        return 0
     if args.calibrate:
         import torch
         import __graft_entry__

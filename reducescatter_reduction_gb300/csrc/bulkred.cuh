@@ -171,11 +171,11 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
     a.stall_test = 0;
 
     auto kern = bulkred_kernel<T, OP, P>;
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<bool> attr{false};  // set once; racing first calls both set it
+    if (!attr.load(std::memory_order_acquire)) {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTmaSmemLimit));
         if (err != cudaSuccess) return err;
-        attr = true;
+        attr.store(true, std::memory_order_release);
     }
     uint64_t cap;
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) {

@@ -7,6 +7,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "internal.h"
@@ -34,6 +35,18 @@ __device__ __forceinline__ void st_v4(void *p, const uint4 &v)
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
                  : "memory");
+}
+
+// Keeps a batch of loads in flight: an empty volatile asm that "modifies"
+// every loaded register.  Volatile asm statements keep their order, so all of
+// the batch's loads are issued before the first value is consumed (without
+// it the compiler may interleave each load with its fold and keep only one or
+// two loads outstanding).
+template <int N>
+__device__ __forceinline__ void hold_batch(uint4 (&r)[N])
+{
+#pragma unroll
+    for (int k = 0; k < N; ++k) asm volatile("" : "+r"(r[k].x), "+r"(r[k].y), "+r"(r[k].z), "+r"(r[k].w));
 }
 
 // Results are written once and not read again by this kernel: streaming

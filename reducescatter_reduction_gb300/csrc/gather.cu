@@ -91,11 +91,11 @@ static cudaError_t gather_launch(const Launch &L, LaunchInfo *info)
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) {
         cap = uint64_t(L.sm_budget);
         smem = 120 * 1024;  // at most one CTA per SM
-        static bool attr = false;
-        if (!attr) {
+        static std::atomic<bool> attr{false};  // set once; racing first calls both set it
+        if (!attr.load(std::memory_order_acquire)) {
             cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
             if (err != cudaSuccess) return err;
-            attr = true;
+            attr.store(true, std::memory_order_release);
         }
     }
     const int grid = int(want < cap ? want : cap);

@@ -197,11 +197,11 @@ static cudaError_t launch_p(const Launch &L, LaunchInfo *info)
         // SM's shared memory so that no two fit on one SM
         cap = uint64_t(L.sm_budget);
         smem = 120 * 1024;
-        static bool attr = false;
-        if (!attr) {
+        static std::atomic<bool> attr{false};  // set once; racing first calls both set it
+        if (!attr.load(std::memory_order_acquire)) {
             cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
             if (err != cudaSuccess) return err;
-            attr = true;
+            attr.store(true, std::memory_order_release);
         }
     }
     const int grid = int(want < cap ? want : cap);

@@ -114,9 +114,23 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
             float acc[VEC], v[VEC];
             if constexpr (P > 0) {
                 uint4 r[P];
+                if constexpr (THREADS <= 128) {
+                    // decode (few rows): all p loads in flight before the first
+                    // fold -- 3.89 vs 4.03 us per decode call on GB300
+                    const char *sp[P];
 #pragma unroll
-                for (int k = 0; k < P; ++k)
-                    r[k] = ld_stream_v4(static_cast<const char *>(a.src[a.order[c][k]]) + e * S);
+                    for (int k = 0; k < P; ++k) sp[k] = static_cast<const char *>(a.src[a.order[c][k]]) + e * S;
+#pragma unroll
+                    for (int k = 0; k < P; ++k) r[k] = ld_stream_v4(sp[k]);
+                    hold_batch(r);
+                } else {
+                    // many rows: the compiler's interleaved schedule uses fewer
+                    // registers and keeps more CTAs resident -- 193 vs 202 us at
+                    // 4096 tokens
+#pragma unroll
+                    for (int k = 0; k < P; ++k)
+                        r[k] = ld_stream_v4(static_cast<const char *>(a.src[a.order[c][k]]) + e * S);
+                }
                 Tr::unpack(r[0], acc);
 #pragma unroll
                 for (int k = 1; k < P; ++k) {

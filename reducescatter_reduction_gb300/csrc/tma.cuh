@@ -354,11 +354,11 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
     a.stall_test = L.stall_test;
 
     auto kern = tma_reduce_kernel<T, OP, P, MODE>;
-    static size_t attr_smem = 0;
-    if (attr_smem < smem) {
+    static std::atomic<bool> attr{false};  // set once; racing first calls both set it
+    if (!attr.load(std::memory_order_acquire)) {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTmaSmemLimit));
         if (err != cudaSuccess) return err;
-        attr_smem = kTmaSmemLimit;
+        attr.store(true, std::memory_order_release);
     }
     uint64_t cap = uint64_t(L.num_sms);
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) cap = uint64_t(L.sm_budget);
