@@ -194,22 +194,21 @@ extern "C" ccl_schedule_t ccl_select_schedule(int p, double nbytes, const ccl_co
     return (ta >= 0 && ta < tr) ? CCL_SCHED_ALLPAIRS : CCL_SCHED_RING;
 }
 
-// Launch lookup table (T-CCL, section "Launch Configuration Tuning": measured
-// configurations ranked per collective and message size).  Per-call device
-// time of the p=8 bf16 AllReduce on GB300 (bench.py --calibrate, CUDA-graph
-// replay), ld/st vs TMA under an SM budget: bytes per rank from which TMA is
-// the faster variant.
-//   budget  8: 256 KiB: 8.25 vs 8.31 us, 1 MiB: 27.2 vs 25.3 us
-//   budget 16: 256 KiB: 5.08 vs 5.66 us, 1 MiB: 14.6 vs 14.0 us
-//   budget 32: 1 MiB:   8.51 vs 8.43 us
-//   budget 76: 1 MiB:   5.24 vs 5.69 us, 4 MiB: 21.3 vs 13.4 us
-static double tma_crossover_bytes(int sm_budget)
+// Launch choice (T-CCL, section "Launch Configuration Tuning": measured
+// configurations ranked per message size).  Per-call device time on GB300
+// (bench.py --calibrate, p=8 bf16; bench.py "sm_budgets", p=16 bf16 224 MiB):
+//   every SM:        ld/st at every size (p=8, 256 MiB: 610 vs 661 us for TMA)
+//   8 .. 32 SMs:     ld/st, one large CTA per SM (~102 vs ~75 GB/s per SM)
+//   76 SMs, p=8:     TMA from 64 MiB per rank (164 vs 178 us; 639 vs 712 at
+//                    256 MiB): one register-staged CTA per SM keeps too few
+//                    bytes in flight once half the GPU nears the HBM peak
+//   76 SMs, p=16:    ld/st (6825 vs 5611 GB/s)
+// So AUTO takes the TMA variant only at p <= 8, on at least half of the SMs
+// (but not all), for 32 MiB per rank and more, where its layout allows it.
+static bool auto_prefers_tma(int p, int sm_budget, int num_sms, double bytes_per_rank)
 {
-    static const struct { int budget; double bytes; } lut[] = {
-        {8, 256.0 * 1024}, {16, 1024.0 * 1024}, {32, 1024.0 * 1024}, {76, 2048.0 * 1024}};
-    for (const auto &row : lut)
-        if (sm_budget <= row.budget) return row.bytes;
-    return 2048.0 * 1024;
+    return p <= 8 && sm_budget > 0 && sm_budget < num_sms && 2 * sm_budget >= num_sms &&
+           bytes_per_rank >= 32.0 * 1024 * 1024;
 }
 
 static int resolve_schedule(const ccl_comm *c, int schedule, double nbytes)
@@ -427,17 +426,13 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     if (coll != COLL_AR && n % size_t(p) != 0)
         return fail(CCL_ERR_INVALID_ARG, "%s needs n %% p == 0 (n=%zu, p=%d)", kCollName[coll], n, p);
     if (n > (SIZE_MAX / 2) / s) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
-    // AUTO: with every SM available the ld/st kernel is faster (7.05 vs 6.26
-    // TB/s at p=16 on GB300); under an SM budget the TMA pipeline moves about
-    // 1.8x more bytes per SM (75 vs 41 GB/s per SM), but its set-up costs
-    // about 1 us more per call, so it is chosen above the budget's measured
-    // crossover (tma_crossover_bytes) when the layout allows it.  AllGather has
-    // only the ld/st kernel.
+    // AUTO: the ld/st kernel, or the TMA variant where auto_prefers_tma says
+    // it is measured faster and the layout allows it.  AllGather has only the
+    // ld/st kernel.
     int variant = c->variant;
     if (variant == CCL_VARIANT_AUTO) {
         variant = CCL_VARIANT_LDST;
-        if (coll != COLL_AG && c->sm_budget > 0 && c->sm_budget < c->num_sms && n > 0 &&
-            double(n) * double(s) >= tma_crossover_bytes(c->sm_budget)) {
+        if (coll != COLL_AG && n > 0 && auto_prefers_tma(p, c->sm_budget, c->num_sms, double(n) * double(s))) {
             uint64_t bounds[kMaxRanks + 1];
             chunk_bounds(p, n, bounds);
             bool ok = true;

@@ -10,7 +10,8 @@
 
 namespace ccl {
 
-constexpr int kGatherThreads = 256;
+constexpr int kGatherThreads = 256;        // whole GPU: one unit per thread
+constexpr int kGatherBudgetThreads = 1024; // SM budget: one persistent CTA per SM carries its load queue
 
 template <int PM>
 struct GatherArgs {
@@ -39,8 +40,8 @@ template <> struct Unit<2> {
     __device__ static void store(char *p, uint16_t v) { *reinterpret_cast<uint16_t *>(p) = v; }
 };
 
-template <int P, int U>
-__global__ void __launch_bounds__(kGatherThreads)
+template <int P, int U, int THREADS>
+__global__ void __launch_bounds__(THREADS, 1)
     gather_kernel(const __grid_constant__ GatherArgs<(P > 0 ? P : kMaxRanks)> a)
 {
     const int p = P > 0 ? P : a.p;
@@ -82,13 +83,18 @@ static cudaError_t gather_launch(const Launch &L, LaunchInfo *info)
     a.p = L.p;
     a.self_mask = L.self_mask;
 
-    auto kern = gather_kernel<P, U>;
+    // the persistent large-CTA kernel only when the message does not already
+    // fit in at most `budget` small CTAs
+    const uint64_t small_grid = (a.nunits + kGatherThreads - 1) / kGatherThreads;
+    const bool budget = L.sm_budget > 0 && L.sm_budget < L.num_sms && small_grid > uint64_t(L.sm_budget);
+    auto kern = budget ? gather_kernel<P, U, kGatherBudgetThreads> : gather_kernel<P, U, kGatherThreads>;
+    const int threads = budget ? kGatherBudgetThreads : kGatherThreads;
     // one unit per thread; the block scheduler streams CTAs through the SMs
-    uint64_t want = (a.nunits + kGatherThreads - 1) / kGatherThreads;
+    uint64_t want = (a.nunits + threads - 1) / threads;
     if (want < 1) want = 1;
     uint64_t cap = uint64_t(0x7fffffff);
     size_t smem = 0;
-    if (L.sm_budget > 0 && L.sm_budget < L.num_sms) {
+    if (budget) {
         cap = uint64_t(L.sm_budget);
         smem = 120 * 1024;  // at most one CTA per SM
         static std::atomic<bool> attr{false};  // set once; racing first calls both set it
@@ -99,11 +105,11 @@ static cudaError_t gather_launch(const Launch &L, LaunchInfo *info)
         }
     }
     const int grid = int(want < cap ? want : cap);
-    kern<<<grid, kGatherThreads, smem, L.stream>>>(a);
+    kern<<<grid, threads, smem, L.stream>>>(a);
     if (info) {
         info->kernel = "all_gather_ldst";
         info->grid = grid;
-        info->block = kGatherThreads;
+        info->block = threads;
         info->smem = smem;
         info->kernels = 1;
     }

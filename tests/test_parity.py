@@ -485,20 +485,31 @@ def test_cuda_graph_capture_and_replay(variant):
         ccl.ccl_comm_check(cm.h)
 
 
-def test_auto_variant_follows_sm_budget():
-    """AUTO follows the measured launch table: ld/st with every SM; under a
-    16-SM budget, ld/st below 1 MiB per rank and TMA from there on."""
-    p, n = 16, 16 * 65536                                 # 2 MiB per rank
+def test_auto_variant_and_budget_kernels():
+    """AUTO runs the ld/st kernel, except at p <= 8 on at least half of the SMs
+    (not all) for 32 MiB per rank and more, where the TMA variant is measured
+    faster.  Under a budget a large ld/st message runs one 512/1024-thread CTA
+    per SM; a message that already fits in `budget` small CTAs keeps the
+    regular kernel."""
+    p, n = 16, 16 * 65536                                 # 2 MiB per rank: 131072 groups
     xs = gen("bf16", "sum", p, n, seed=52)
     _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto")
-    assert "variant=ldst" in desc
+    assert "variant=ldst" in desc and "block=128" in desc
     _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
-    assert "variant=tma" in desc and "grid=16" in desc
-    small = gen("bf16", "sum", p, 16 * 8192, seed=54)     # 256 KiB per rank
-    _, desc = run_collective(small, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
-    assert "variant=ldst" in desc and "grid=16" in desc
-    xs = gen("bf16", "sum", 4, 4 * 1001, seed=53)       # chunks off the 16-byte grid: ld/st
-    _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
+    assert "variant=ldst" in desc and "grid=16 block=512" in desc
+    small = gen("bf16", "sum", p, 16 * 64, seed=54)       # 2 KiB per rank: one 128-thread CTA
+    res, desc = run_collective(small, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
+    assert "variant=ldst" in desc and "grid=1 block=128" in desc
+    want = oracle.allreduce(small, "sum", "bf16", "ring")
+    assert bits_equal(res.host(3), want[3])
+    half = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    big = gen("bf16", "sum", 8, 1 << 24, seed=55)         # 32 MiB per rank
+    _, desc = run_collective(big, "ar", "sum", "bf16", "ring", variant="auto", budget=half)
+    assert "variant=tma" in desc
+    _, desc = run_collective(big, "ar", "sum", "bf16", "ring", variant="auto", budget=32)
+    assert "variant=ldst" in desc and "block=1024" in desc
+    _, desc = run_collective([x[: 1 << 23] for x in big], "ar", "sum", "bf16", "ring",
+                             variant="auto", budget=half)   # 16 MiB per rank
     assert "variant=ldst" in desc
 
 
