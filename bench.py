@@ -68,6 +68,9 @@ def parse_args(argv=None):
     ap.add_argument("--rmsnorm-tokens", type=int, default=0,
                     help="profiling mode: only the fused AllReduce + residual + RMSNorm, p=8 bf16, "
                          "[tokens, 8192], warmup + steps calls")
+    ap.add_argument("--moe-rows", type=int, default=0,
+                    help="profiling mode: only the p=16 bf16 [rows, 7168] ring AllReduce with --variant and "
+                         "--sm-budget, warmup + steps calls")
     ap.add_argument("--calibrate", action="store_true",
                     help="fit t = alpha + bytes/B per variant and SM budget (p=8 bf16) and print the table")
     ap.add_argument("--n", type=int, default=N,
@@ -356,10 +359,11 @@ def run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes, n):
     pinned host memory, runs the AllReduce through the C ABI, and copies its
     p results back to pinned host memory, all inside the timed region.
 
-    value: a stream of such steps, double-buffered (two device buffer sets;
-    host->device copies on one stream, AllReduce on another, device->host on a
-    third, ordered by events), so that step i+1's input copy overlaps step i's
-    AllReduce and output copy.  serial: one step at a time on one stream."""
+    Two ways of running a stream of such steps are timed: double-buffered (two
+    device buffer sets; host->device copies on one stream, AllReduce on
+    another, device->host on a third, ordered by events), so that step i+1's
+    input copy overlaps step i's AllReduce and output copy; and serial, one
+    step at a time on one stream.  value is the faster of the two."""
     import torch
     import reducescatter_reduction_gb300 as ccl
 
@@ -434,11 +438,17 @@ def run_e2e(args, dist, comm, ins, outs, sptr, stream, alg_bytes, n):
     ccl.ccl_comm_destroy(comm2)
     t_ms, _, gbs = aggregate(dist, t_piped, alg_bytes * args.e2e_steps)
     ts_ms, _, gbs_serial = aggregate(dist, t_serial, alg_bytes * args.e2e_steps)
-    return {"value": round(gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": P * n * S,
+    piped = {"value": round(gbs, 2), "ms_per_step": round(t_ms / args.e2e_steps, 4),
+             "mode": "double-buffered: H2D, AllReduce and D2H on three streams"}
+    serial = {"value": round(gbs_serial, 2), "ms_per_step": round(ts_ms / args.e2e_steps, 4),
+              "mode": "serial: H2D, AllReduce, D2H on one stream"}
+    # Both run the same calls on the same host buffers; which one is faster
+    # depends on how the machine's host link takes both directions at once,
+    # so the line reports the faster and keeps the other beside it.
+    best, other = (piped, serial) if gbs >= gbs_serial else (serial, piped)
+    return {"value": best["value"], "unit": "GB/s", "h2d_bytes_per_step": P * n * S,
             "d2h_bytes_per_step": P * n * S, "steps": args.e2e_steps,
-            "ms_per_step": round(t_ms / args.e2e_steps, 4),
-            "mode": "double-buffered: H2D, AllReduce and D2H on three streams",
-            "serial": {"value": round(gbs_serial, 2), "ms_per_step": round(ts_ms / args.e2e_steps, 4)}}
+            "ms_per_step": best["ms_per_step"], "mode": best["mode"], "other_mode": other}
 
 
 def run_variants(comm, sptr, stream, peak, n, args):
@@ -929,6 +939,36 @@ def main(argv=None):
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / max(1, args.steps)
         print(json.dumps({"mode": "rmsnorm", "tokens": tokens, "us_per_call": round(us, 2),
+                          "launch": ccl.ccl_comm_last_launch(h)}), flush=True)
+        ccl.ccl_comm_destroy(h)
+        return 0
+    if args.moe_rows:
+        import torch
+        import __graft_entry__
+        import reducescatter_reduction_gb300 as ccl
+        __graft_entry__.build()
+        dev = torch.device("cuda", dist.local_rank)
+        p, n = 16, args.moe_rows * 7168
+        ins = [torch.randn(n, device=dev, dtype=torch.float32).to(torch.bfloat16) for _ in range(p)]
+        outs = [torch.empty_like(t) for t in ins]
+        h = ccl.ccl_comm_create(p, [t.data_ptr() for t in ins])
+        ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
+        ccl.ccl_set_launch(h, args.sm_budget, args.variant, 0)
+        s = torch.cuda.current_stream()
+        for _ in range(args.warmup):
+            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s.cuda_stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s.cuda_stream)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / max(1, args.steps)
+        ccl.ccl_comm_check(h)
+        print(json.dumps({"mode": "moe", "rows": args.moe_rows, "variant": args.variant,
+                          "sm_budget": args.sm_budget, "us_per_call": round(us, 2),
+                          "GBps": round(2 * p * n * S / (us * 1e-6) / 1e9, 1),
                           "launch": ccl.ccl_comm_last_launch(h)}), flush=True)
         ccl.ccl_comm_destroy(h)
         return 0

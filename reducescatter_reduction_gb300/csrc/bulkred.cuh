@@ -24,7 +24,15 @@
 
 namespace ccl {
 
-constexpr int kBulkThreads = 64;  // warp 0: producer lane; warp 1: issuer lane
+constexpr int kBulkThreads = 64;  // one pipe: warp 0's lane 0 loads, warp 1's lane 0 issues
+constexpr int kBulkMaxPipes = 4;
+
+// Shared memory of one pipe: S stages of p tiles, its full/empty barriers and
+// its control block, rounded up to 128 bytes so every pipe starts aligned.
+__host__ __device__ constexpr size_t bulkred_pipe_bytes(int p, uint32_t tile, uint32_t stages)
+{
+    return (size_t(stages) * size_t(p) * tile + 2 * size_t(stages) * 8 + kTmaCtlBytes + 127) / 128 * 128;
+}
 
 template <typename T, int OP> struct BulkRed;
 
@@ -58,20 +66,28 @@ template <typename T, int OP> struct BulkRed {
 
 // dst[c] is where chunk c's reduction goes: the RS output of rank c, or, for
 // an AllReduce, rank c's output at the chunk's offset.
+//
+// A CTA runs blockDim.x / 64 independent pipes, each on its own shared-memory
+// region and its own tiles (pipe j of CTA b takes tiles b*K + j, stepping by
+// gridDim.x*K).  The issuing lane's wait for each tile's first store to land
+// serialises one pipe; several pipes per CTA keep several tiles' reductions in
+// flight on one SM, which is what an SM budget (one CTA per SM) needs.
 template <typename T, int OP, int P>
-__global__ void __launch_bounds__(kBulkThreads)
+__global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
     bulkred_kernel(const __grid_constant__ TmaArgs<(P > 0 ? P : kMaxRanks)> a)
 {
     constexpr int S_ELEM = (Traits<T>::VEC == 8) ? 2 : 4;
     extern __shared__ __align__(128) unsigned char smem[];
     const int p = P > 0 ? P : a.p;
     const uint32_t TB = a.tile_bytes, S = a.stages;
-    unsigned char *in_base = smem;                                       // [S][p][TB]
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(S) * p * TB);
+    const uint32_t K = blockDim.x / kBulkThreads, j = threadIdx.x / kBulkThreads;
+    const uint32_t lt = threadIdx.x % kBulkThreads;
+    unsigned char *in_base = smem + size_t(j) * bulkred_pipe_bytes(p, TB, S);   // [S][p][TB]
+    uint64_t *full = reinterpret_cast<uint64_t *>(in_base + size_t(S) * p * TB);
     uint64_t *empty = full + S;
     volatile TmaCtl *ctl = reinterpret_cast<volatile TmaCtl *>(empty + S);
 
-    if (threadIdx.x == 0) {
+    if (lt == 0) {
         for (uint32_t s = 0; s < S; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), 1);
@@ -85,11 +101,12 @@ __global__ void __launch_bounds__(kBulkThreads)
     __syncthreads();
 
     const uint64_t ntiles = a.tstart[p];
-    if (threadIdx.x == 0) {
+    const uint64_t first = uint64_t(blockIdx.x) * K + j, step = uint64_t(gridDim.x) * K;
+    if (lt == 0) {
         // producer
         int c = 0;
         uint32_t i = 0;
-        for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+        for (uint64_t t = first; t < ntiles; t += step, ++i) {
             const uint32_t s = i % S;
             if (i >= S && !bounded_wait(a, ctl, smem_addr(&empty[s]), ((i / S) - 1) & 1u, 2u, t)) break;
             while (t >= a.tstart[c + 1]) ++c;
@@ -104,11 +121,11 @@ __global__ void __launch_bounds__(kBulkThreads)
                           bytes, bar);
             ctl->issued = i + 1;
         }
-    } else if (threadIdx.x == 32) {
+    } else if (lt == 32) {
         // issuer
         int c = 0;
         uint32_t i = 0;
-        for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+        for (uint64_t t = first; t < ntiles; t += step, ++i) {
             const uint32_t s = i % S;
             if (!bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, t)) break;
             while (t >= a.tstart[c + 1]) ++c;
@@ -129,12 +146,12 @@ __global__ void __launch_bounds__(kBulkThreads)
         bulk_wait_all();
     }
     __syncthreads();
-    if (threadIdx.x == 0 && ctl->abort) {
+    if (lt == 0 && ctl->abort) {
         const uint32_t issued = ctl->issued;
-        for (uint32_t j = ctl->consumed; j < issued; ++j) {
-            const uint32_t bar = smem_addr(&full[j % S]);
+        for (uint32_t q = ctl->consumed; q < issued; ++q) {
+            const uint32_t bar = smem_addr(&full[q % S]);
             const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(bar, (j / S) & 1u))
+            while (!mbar_try_wait(bar, (q / S) & 1u))
                 if (global_ns() - t0 > uint64_t(a.wait_ns)) break;
         }
     }
@@ -177,23 +194,33 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
         if (err != cudaSuccess) return err;
         attr.store(true, std::memory_order_release);
     }
+    const size_t pipe = bulkred_pipe_bytes(L.p, tile, stages);
     uint64_t cap;
+    uint32_t pipes = 1;
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) {
-        // one CTA per SM: more than half of an SM's shared memory each
-        cap = uint64_t(L.sm_budget);
+        // one CTA per SM (more than half of an SM's shared memory each), with
+        // as many pipes as its shared memory holds
+        pipes = uint32_t(kTmaSmemLimit / pipe);
+        if (pipes > uint32_t(kBulkMaxPipes)) pipes = kBulkMaxPipes;
+        if (pipes < 1) pipes = 1;
+        smem = pipes * pipe;
         if (smem < 120 * 1024) smem = 120 * 1024;
+        cap = uint64_t(L.sm_budget);
     } else {
+        smem = pipe;
         int per_sm = 0;
         cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBulkThreads, smem);
         if (err != cudaSuccess) return err;
         cap = uint64_t(L.num_sms) * (per_sm > 0 ? per_sm : 1);
     }
-    const int grid = int(tiles < cap ? (tiles ? tiles : 1) : cap);
-    kern<<<grid, kBulkThreads, smem, L.stream>>>(a);
+    const uint64_t ctas = (tiles + pipes - 1) / pipes;
+    const int grid = int(ctas < cap ? (ctas ? ctas : 1) : cap);
+    const int block = int(pipes) * kBulkThreads;
+    kern<<<grid, block, smem, L.stream>>>(a);
     if (info) {
         info->kernel = MODE_AR == L.mode ? "allreduce_tma_bulkred" : "reduce_scatter_tma_bulkred";
         info->grid = grid;
-        info->block = kBulkThreads;
+        info->block = block;
         info->smem = smem;
         info->kernels = 1;
     }

@@ -187,10 +187,13 @@ def test_reduce_scatter_in_place_nccl_convention(dtype):
 
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("inplace", [False, True])
-def test_all_gather(dtype, inplace):
+@pytest.mark.parametrize("budget", [0, 3])
+def test_all_gather(dtype, inplace, budget):
+    """Budget 3: the persistent kernel (several units per thread per round)
+    wherever the message needs more than three small CTAs."""
     for p, n in ((2, 2 * 4099), (3, 3 * 1000), (8, 8 * 65536), (16, 16 * 513), (5, 5 * 8)):
         xs = gen(dtype, "sum", p, n, seed=13)
-        res, _ = run_collective(xs, "ag", None, dtype, inplace=inplace)
+        res, _ = run_collective(xs, "ag", None, dtype, inplace=inplace, budget=budget)
         want = oracle.all_gather(xs, dtype)
         for r in range(p):
             assert bits_equal(res.host(r), want[r]), (p, r)

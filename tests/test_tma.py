@@ -202,6 +202,27 @@ def test_bulkred_exact_ops_match_oracle(dtype, op):
             assert bits_equal(rs.host(r), want[r]), (p, r)
 
 
+@pytest.mark.parametrize("budget", [1, 4])
+def test_bulkred_exact_ops_under_budget_match_oracle(budget):
+    """Under an SM budget one CTA per SM runs several bulk-reduce pipes (up to
+    four, each on its own tiles): int32 sum and bf16 max stay bit-identical to
+    the oracle for every p, including a short last tile and more tiles than
+    pipes x CTAs."""
+    for dtype, op in (("i32", "sum"), ("bf16", "max")):
+        for p in (2, 4, 8, 16, 17):
+            n = tma_sizes(p, dtype)[2]
+            xs = gen(dtype, op, p, n, seed=120 + p)
+            res, desc = run_collective(xs, "ar", op, dtype, "ring", variant="tma_bulkred", budget=budget)
+            assert int(desc.split("grid=")[1].split()[0]) <= budget, desc
+            want = oracle.allreduce(xs, op, dtype, "ring")
+            for r in range(p):
+                assert bits_equal(res.host(r), want[r]), (dtype, p, r, desc)
+            rs, desc = run_collective(xs, "rs", op, dtype, "allpairs", variant="tma_bulkred", budget=budget)
+            want = oracle.reduce_scatter(xs, op, dtype, "allpairs")
+            for r in range(p):
+                assert bits_equal(rs.host(r), want[r]), (dtype, p, r, desc)
+
+
 def test_bulkred_reduce_scatter_in_place_and_budget():
     p, dtype = 8, "bf16"
     n = p * (1 << 18)
