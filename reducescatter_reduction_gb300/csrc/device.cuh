@@ -9,6 +9,7 @@
 
 #include <atomic>
 #include <type_traits>
+#include <utility>
 
 #include "internal.h"
 
@@ -57,6 +58,37 @@ __device__ __forceinline__ void st_stream_v4(void *p, const uint4 &v)
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
                  : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch (sm_90 and later).  A kernel launched with
+// launch_dependent may be scheduled while the kernel before it in the stream
+// is still draining; before its first global memory access it waits, with
+// grid_dependency_wait, until that kernel has completed and its writes are
+// visible.  grid_dependents_launch lets the next such kernel be scheduled
+// once every CTA of this grid has issued it (or exited); it changes only
+// when the next kernel is scheduled, never what it may read.  Both
+// instructions do nothing in a kernel launched the ordinary way.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                                    cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------

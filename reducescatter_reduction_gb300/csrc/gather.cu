@@ -44,6 +44,8 @@ template <int P, int U, int THREADS>
 __global__ void __launch_bounds__(THREADS, 1)
     gather_kernel(const __grid_constant__ GatherArgs<(P > 0 ? P : kMaxRanks)> a)
 {
+    grid_dependency_wait();
+    if (THREADS == kGatherThreads) grid_dependents_launch();  // not in the persistent SM-budget kernel
     const int p = P > 0 ? P : a.p;
     const uint64_t tid = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
@@ -105,7 +107,8 @@ static cudaError_t gather_launch(const Launch &L, LaunchInfo *info)
         }
     }
     const int grid = int(want < cap ? want : cap);
-    kern<<<grid, threads, smem, L.stream>>>(a);
+    cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(threads), smem, L.stream, a);
+    if (err != cudaSuccess) return err;
     if (info) {
         info->kernel = "all_gather_ldst";
         info->grid = grid;

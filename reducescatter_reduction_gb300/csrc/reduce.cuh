@@ -171,18 +171,24 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
 
 // Whole GPU: the compiler's own register choice (62 at p=8 bf16: four
 // 256-thread CTAs per SM).
+// Launched as a dependent: the next kernel may be scheduled once the last
+// wave of CTAs is running.
 template <typename T, int OP, int P, int MODE>
 __global__ void __launch_bounds__(reduce_threads<P>())
     reduce_kernel(const __grid_constant__ ReduceArgs<(P > 0 ? P : kMaxRanks)> a)
 {
+    grid_dependency_wait();
+    grid_dependents_launch();
     reduce_body<T, OP, P, MODE>(a);
 }
 
 // SM budget: one large CTA per SM, so the full register file per thread.
+// Persistent, so the next kernel is scheduled only as its CTAs exit.
 template <typename T, int OP, int P, int MODE>
 __global__ void __launch_bounds__(reduce_budget_threads<P>(), 1)
     reduce_budget_kernel(const __grid_constant__ ReduceArgs<(P > 0 ? P : kMaxRanks)> a)
 {
+    grid_dependency_wait();
     reduce_body<T, OP, P, MODE>(a);
 }
 
@@ -232,7 +238,8 @@ static cudaError_t launch_p(const Launch &L, LaunchInfo *info)
         }
     }
     const int grid = int(want < cap ? want : cap);
-    kern<<<grid, kThreads, smem, L.stream>>>(a);
+    cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(kThreads), smem, L.stream, a);
+    if (err != cudaSuccess) return err;
     if (info) {
         info->kernel = MODE == MODE_AR ? "allreduce_ldst" : "reduce_scatter_ldst";
         info->grid = grid;

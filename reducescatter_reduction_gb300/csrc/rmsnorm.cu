@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
     constexpr int S = (VEC == 8) ? 2 : 4;
     __shared__ float red[32];
     __shared__ float slice_sum;
+    grid_dependency_wait();
+    grid_dependents_launch();
     cg::cluster_group cluster = cg::this_cluster();
     const int C = int(cluster.num_blocks());
     const int q = int(cluster.block_rank());
@@ -238,13 +240,15 @@ static cudaError_t norm_launch(const Launch &L, const NormLaunch &N, LaunchInfo 
     cfg.blockDim = dim3(unsigned(threads));
     cfg.dynamicSmemBytes = 0;
     cfg.stream = L.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(C);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // launched as a dependent
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = unsigned(C);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = C > 1 ? 1 : 0;  // one CTA per row: no cluster needed
+    cfg.numAttrs = C > 1 ? 2 : 1;  // one CTA per row: no cluster needed
     cudaError_t err = few_rows ? cudaLaunchKernelEx(&cfg, ar_rmsnorm_kernel<T, P, 128>, a)
                                : cudaLaunchKernelEx(&cfg, ar_rmsnorm_kernel<T, P, kNormMaxThreads>, a);
     if (err != cudaSuccess) return err;

@@ -488,6 +488,69 @@ def test_cuda_graph_capture_and_replay(variant):
         ccl.ccl_comm_check(cm.h)
 
 
+def _dependent_chain_oracle(xs):
+    y = oracle.allreduce(xs, "sum", "f32", "ring")
+    y[0] = y[0] * np.float32(2.0)
+    y = oracle.allreduce(y, "max", "f32", "allpairs")
+    y = oracle.allreduce(y, "sum", "f32", "ring")
+    rs = oracle.reduce_scatter(y, "sum", "f32", "ring")
+    chunk = len(rs[0])
+    return y, [np.concatenate(rs) for _ in rs], chunk
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_dependent_launch_chain(graph):
+    """The ld/st, AllGather and fused kernels are launched as programmatic
+    dependents: each may be scheduled while the kernel before it drains, and
+    waits for that kernel's writes before touching memory.  A chain of
+    collectives, each reading what the previous one wrote (with an ordinary
+    torch kernel in between), issued back to back without synchronising,
+    must give the oracle's chain bit for bit, on a stream and in a CUDA graph."""
+    p, n = 8, 8 * 65536                                # one wave of CTAs: every CTA starts at once
+    xs = gen("f32", "sum", p, n, seed=56)
+    ins = RankBuffers(xs, n, np.float32)
+    b = RankBuffers(None, n, np.float32, p=p)
+    c = RankBuffers(None, n, np.float32, p=p)
+    d = RankBuffers(None, n, np.float32, p=p)
+    want_b, want_d, chunk = _dependent_chain_oracle(xs)
+    with Comm(ins, b) as cm_ab, Comm(b, c) as cm_bc, Comm(c, b) as cm_cb, \
+            Comm(b, out_ptrs=[d.ptr(r, r * (n // p)) for r in range(p)]) as cm_bd:
+        ccl.ccl_set_launch(cm_cb.h, 3, "ldst", 0)                 # the persistent SM-budget kernel
+        # the AllGather runs in place on D: its rank buffers are D itself
+        ag = ccl.ccl_comm_create(p, d.ptrs())
+        try:
+            def chain(s):
+                ccl.ccl_allreduce(cm_ab.h, "sum", "f32", n, "ring", s)
+                with torch.cuda.stream(torch.cuda.ExternalStream(s)):
+                    b.views[0].view(torch.float32).mul_(2.0)
+                ccl.ccl_allreduce(cm_bc.h, "max", "f32", n, "allpairs", s)
+                ccl.ccl_allreduce(cm_cb.h, "sum", "f32", n, "ring", s)
+                ccl.ccl_reduce_scatter(cm_bd.h, "sum", "f32", n, "ring", s)
+                ccl.ccl_all_gather(ag, "f32", n, s)
+            if graph:
+                chain(stream_ptr())                                 # first use outside the capture
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream()
+                side.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(side):
+                    with torch.cuda.graph(g, stream=side):
+                        chain(torch.cuda.current_stream().cuda_stream)
+                torch.cuda.current_stream().wait_stream(side)
+                for _ in range(2):
+                    g.replay()
+            else:
+                for _ in range(2):
+                    chain(stream_ptr())
+            torch.cuda.synchronize()
+        finally:
+            ccl.ccl_comm_destroy(ag)
+    for r in range(p):
+        assert bits_equal(b.host(r), want_b[r]), r
+        assert bits_equal(d.host(r), want_d[r]), r
+    assert ins.guards_intact() and b.guards_intact() and c.guards_intact() and d.guards_intact()
+
+
 def test_auto_variant_and_budget_kernels():
     """AUTO runs the ld/st kernel, except at p <= 8 on at least half of the SMs
     (not all) for 32 MiB per rank and more, where the TMA variant is measured
