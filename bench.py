@@ -582,7 +582,7 @@ def calibrate(dev):
 
 def run_rmsnorm(dev, peak):
     """AllReduce fused with the residual merge and RMSNorm at TP=8 (p=8 bf16,
-    hidden 8192), decode (1 token) and prefill (4096 tokens), against the
+    hidden 8192) at 1, 32, 256 and 4096 tokens, against the
     AllReduce alone and against the AllReduce followed by the same epilogue in
     torch on one rank's copy (a lower bound for the unfused path, which would
     also write p outputs).  Per-call device time from CUDA-graph replay."""
@@ -591,7 +591,7 @@ def run_rmsnorm(dev, peak):
 
     p, hidden = 8, 8192
     rows_out = {}
-    for tokens in (1, 4096):
+    for tokens in (1, 32, 256, 4096):
         n = tokens * hidden
         ins = [(0.02 * torch.randn(n, device=dev)).to(torch.bfloat16) for _ in range(p)]
         outs = [torch.empty_like(t) for t in ins]

@@ -8,7 +8,7 @@
 //   out = round(h * (1 / sqrt(mean(h^2) + eps)) * gamma)   written to every rank
 // A thread-block cluster of C CTAs per row, each CTA a slice of the columns
 // (for decode, C up to 8 so that a row of 8192 columns is spread over 1024
-// threads; for many rows, one 512-thread CTA per row).  Pass 1 folds the p inputs, merges the residual, stores h and
+// threads; for many rows, one CTA per row).  Pass 1 folds the p inputs, merges the residual, stores h and
 // accumulates the slice's sum of squares of the rounded h; the C partial sums
 // are combined through distributed shared memory (every CTA adds the same C
 // values in the same order, so all slices use one bit-identical 1/rms), and
@@ -26,7 +26,9 @@ namespace ccl {
 
 namespace cg = cooperative_groups;
 
-constexpr int kNormMaxThreads = 512;
+constexpr int kNormDecodeThreads = 128;
+constexpr int kNormMidThreads = 1024;
+constexpr int kNormPrefillThreads = 256;
 constexpr int kNormMaxCluster = 8;
 
 template <int PM>
@@ -127,8 +129,8 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
                     hold_batch(r);
                 } else {
                     // many rows: the compiler's interleaved schedule uses fewer
-                    // registers and keeps more CTAs resident -- 193 vs 202 us at
-                    // 4096 tokens
+                    // registers and keeps more CTAs resident (measured with
+                    // 512-thread CTAs: 193 vs 202 us at 4096 tokens)
 #pragma unroll
                     for (int k = 0; k < P; ++k)
                         r[k] = ld_stream_v4(static_cast<const char *>(a.src[a.order[c][k]]) + e * S);
@@ -224,14 +226,20 @@ static cudaError_t norm_launch(const Launch &L, const NormLaunch &N, LaunchInfo 
     a.p = L.p;
     a.vec = L.vec ? 1 : 0;
     a.eps = N.eps;
-    // Fewer rows than SMs (decode): latency rules, so 128-thread CTAs in a
-    // cluster of up to 8 per row, one unit per thread.  Many rows (prefill):
-    // bytes rule, so 512-thread CTAs, about two units per thread, a cluster
-    // only when a row needs more than one CTA.
+    // CTA shape by rows against the SM count; a row takes a cluster of C CTAs
+    // only when it needs more than one.  Measured on GB300 (p=8 bf16, hidden
+    // 8192, per call, CUDA-graph replay):
+    //   rows < SMs (decode): 128 threads, one unit each, up to 8 CTAs a row --
+    //     latency rules;
+    //   SMs <= rows < 2 SMs: 1024 threads, one unit each -- 256 tokens
+    //     12.96 us against 16.13 with 512 threads x 2 units;
+    //   rows >= 2 SMs (prefill): 256 threads, four units each, so more and
+    //     smaller CTAs per SM overlap one another's block reductions -- 4096
+    //     tokens 188 vs 194 us, 8192 tokens 367 vs 384.
     const uint64_t units = L.vec ? N.hidden / Traits<T>::VEC : N.hidden;
-    const bool few_rows = N.rows < uint64_t(L.num_sms);
-    const int threads = few_rows ? 128 : kNormMaxThreads;
-    const uint64_t per_cta = uint64_t(threads) * (few_rows ? 1 : 2);
+    const uint64_t sms = uint64_t(L.num_sms);
+    const int threads = N.rows < sms ? kNormDecodeThreads : N.rows < 2 * sms ? kNormMidThreads : kNormPrefillThreads;
+    const uint64_t per_cta = uint64_t(threads) * (N.rows < 2 * sms ? 1 : 4);
     const uint64_t want = (units + per_cta - 1) / per_cta;
     const int C = int(want < 1 ? 1 : want > uint64_t(kNormMaxCluster) ? kNormMaxCluster : want);
     if (N.rows * uint64_t(C) > 0x7fffffffull) return cudaErrorInvalidValue;
@@ -249,8 +257,9 @@ static cudaError_t norm_launch(const Launch &L, const NormLaunch &N, LaunchInfo 
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = C > 1 ? 2 : 1;  // one CTA per row: no cluster needed
-    cudaError_t err = few_rows ? cudaLaunchKernelEx(&cfg, ar_rmsnorm_kernel<T, P, 128>, a)
-                               : cudaLaunchKernelEx(&cfg, ar_rmsnorm_kernel<T, P, kNormMaxThreads>, a);
+    cudaError_t err = threads == kNormDecodeThreads ? cudaLaunchKernelEx(&cfg, ar_rmsnorm_kernel<T, P, kNormDecodeThreads>, a)
+                      : threads == kNormMidThreads  ? cudaLaunchKernelEx(&cfg, ar_rmsnorm_kernel<T, P, kNormMidThreads>, a)
+                                                    : cudaLaunchKernelEx(&cfg, ar_rmsnorm_kernel<T, P, kNormPrefillThreads>, a);
     if (err != cudaSuccess) return err;
     const int grid = int(N.rows * C);
     if (info) {

@@ -85,8 +85,15 @@ def test_tp_activation_fused_rmsnorm(dtype, tokens):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("p,rows,hidden,sched", [(3, 5, 1000, "allpairs"), (8, 7, 1023, "ring"),
-                                                 (16, 2, 4096, "allpairs"), (2, 9, 64, "ring")])
+                                                 (16, 2, 4096, "allpairs"), (2, 9, 64, "ring"),
+                                                 (8, 200, 1023, "ring"), (8, 160, 12288, "allpairs"),
+                                                 (3, 400, 1000, "allpairs"), (8, 350, 9216, "ring")])
 def test_fused_rmsnorm_shapes_and_in_place(dtype, p, rows, hidden, sched):
+    """Rows below, between one and two times, and above twice the SM count
+    take the three CTA shapes (128-thread clusters, 1024-thread CTAs,
+    256-thread CTAs with four units per thread); hidden sizes that are not a
+    multiple of 8 take the element path, and 12288 bf16 columns need a
+    two-CTA cluster per row at 1024 threads."""
     n = rows * hidden
     xs = [inputs.normal(n, 5, r, 0.5, dtype) for r in range(p)]
     res = inputs.normal(n, 5, 100, 1.0, dtype)
