@@ -3,9 +3,9 @@
  * all live in the memory of one GPU (NVIDIA GB300, sm_103a).
  *
  * What is computed.  "Inside NCCL AllReduce", section "What all-reduce
- * promises": all-reduce takes one same-shaped buffer per rank, combines them
- * element-wise with sum, prod, min, max or avg, and leaves every rank holding
- * the identical result; it equals a reduce-scatter (each rank ends owning the
+ * promises": all-reduce combines one same-shaped buffer per rank element by
+ * element (sum, prod, min, max or avg), and at the end all ranks hold the same
+ * result; it equals a reduce-scatter (each rank ends owning the
  * finished reduction of one slice) followed by an all-gather (the finished
  * slices go to every rank).  Here the p ranks are p device buffers; there
  * are no peer GPUs and no messages.  Each element is reduced once, in fp32
@@ -224,8 +224,8 @@ CCL_API ccl_status_t ccl_reduce_scatter(ccl_comm_t comm, ccl_op_t op, ccl_dtype_
 CCL_API ccl_status_t ccl_all_gather(ccl_comm_t comm, ccl_dtype_t dtype, size_t n, void *stream);
 
 /* AllReduce fused with the residual merge and RMSNorm, for a tensor-parallel
- * decode step ("Inside NCCL AllReduce", last section: "the merge and the
- * RMSNorm that follow are fused into the preceding all-reduce").  The
+ * decode step ("Inside NCCL AllReduce", last section: the residual merge and
+ * the RMSNorm after the all-reduce run inside the all-reduce kernel).  The
  * communicator's p input buffers are [rows, hidden] row-major (n = rows*hidden
  * elements each).  Per element:
  *   y   = the sum AllReduce of the p inputs, in the schedule's order (fp32,

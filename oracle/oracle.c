@@ -322,9 +322,9 @@ int oracle_allreduce_ring_stepwise(int p, uint64_t n, int dtype, int op, const v
 }
 
 /* AllReduce followed by the merge into the residual stream and RMSNorm,
- * fused in the all-reduce ("Inside NCCL AllReduce", last section: in decoding
- * "the merge and the RMSNorm that follow are fused into the preceding
- * all-reduce").  The pages give no formula; the plain reading, per element of
+ * fused in the all-reduce ("Inside NCCL AllReduce", last section: in a
+ * decoding path the residual merge and the RMSNorm after the all-reduce run
+ * inside the all-reduce kernel).  The pages give no formula; the plain reading, per element of
  * a [rows, hidden] buffer:
  *   y   = the sum AllReduce of the p inputs (schedule order, fp32, rounded)
  *   h   = round(fl32(y) + fl32(residual))            -- the merge

@@ -1,8 +1,8 @@
 // AllReduce fused with the residual merge and RMSNorm.
 //
-// "Inside NCCL AllReduce", last section: in Kimi's decoding path "the merge
-// and the RMSNorm that follow are fused into the preceding all-reduce", so
-// the collective absorbs a kernel.  Per row of a [rows, hidden] buffer:
+// "Inside NCCL AllReduce", last section: in Kimi's decoding path the
+// residual merge and the RMSNorm after the all-reduce run inside the
+// all-reduce kernel, one kernel fewer per layer.  Per row of a [rows, hidden] buffer:
 //   y   = sum AllReduce of the p rank rows (schedule order, fp32, rounded)
 //   h   = round(y + residual)                     written to residual_out
 //   out = round(h * (1 / sqrt(mean(h^2) + eps)) * gamma)   written to every rank

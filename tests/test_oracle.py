@@ -455,7 +455,7 @@ def test_minmax_invariant_under_schedule(dtype, op):
 def test_schedules_differ_only_in_rounding():
     """Ring and all-pairs fold the same terms in different orders: the fp32
     results agree to within the fixed-order bound and do differ somewhere
-    (a different order is not bitwise equal, "MSCCL, in depth", "Failure modes").
+    (reordering changes the bits: "MSCCL, in depth", "Failure modes").
     (bf16 inputs would not show it: p bf16 values sum exactly in fp32.)"""
     p, n = 8, 1 << 14
     xs = inputs.sweep(n, p, dtype="f32")
