@@ -63,7 +63,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-budgets", action="store_true")
     ap.add_argument("--rmsnorm-tokens", type=int, default=0,
                     help="profiling mode: only the fused AllReduce + residual + RMSNorm, p=8 bf16, "
