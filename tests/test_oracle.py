@@ -602,6 +602,24 @@ def test_rmsnorm_closed_form_three_four():
     assert np.array_equal(out, want)
 
 
+def test_rmsnorm_mean_square_is_taken_over_the_stored_merge():
+    """The norm reads h as stored (rounded to the element type), not the fp32
+    merge before rounding.  Hand-checked bf16 row, eps = 0, gamma = 1:
+    y = [2.75, 1.0625, 0.0625, -1.875], residual = [-0.0986328125,
+    -0.2294921875, -0.21484375, -0.2412109375]; the fp32 merge is
+    [2.6513671875, 0.8330078125, -0.15234375, -2.1162109375] and rounds to
+    h = [2.65625, 0.83203125, -0.15234375, -2.109375] (bf16 steps 2^-6 in
+    [2, 4), 2^-8 in [0.5, 1)).  mean(h^2) = 12.220611572265625 / 4, so
+    h0 / rms = 1.51968..., 194.52 steps of 2^-7 -> 1.5234375.  Squaring the
+    unrounded merge instead gives 194.50 steps -> 1.515625."""
+    xs = [to_storage([2.75, 1.0625, 0.0625, -1.875], "bf16"), to_storage([0.0] * 4, "bf16")]
+    res = to_storage([-0.0986328125, -0.2294921875, -0.21484375, -0.2412109375], "bf16")
+    ones = to_storage([1.0] * 4, "bf16")
+    out, h = oracle.allreduce_residual_rmsnorm(xs, res, ones, 1, 4, "bf16", eps=0.0)
+    assert as_float(h, "bf16").tolist() == [2.65625, 0.83203125, -0.15234375, -2.109375]
+    assert as_float(out, "bf16").tolist() == [1.5234375, 0.4765625, -0.0869140625, -1.203125]
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_rmsnorm_constant_rows_give_sign_times_gamma(dtype):
     p, rows, hidden = 4, 3, 64
