@@ -64,8 +64,12 @@
  * AllGather, (n/p) * element size a multiple of 16) take the 128-bit vector
  * path; other layouts take a correct element-wise path (no error).
  *
- * Threads.  A communicator must not be used from two host threads at once.
- * ccl_last_error() is per host thread.
+ * Threads and streams.  A communicator must not be used from two host
+ * threads at once.  Its collectives must also be ordered on the device: issue
+ * them on one stream, or order the streams.  The TMA variants hand out tiles
+ * from a counter in the communicator's status block, so two collectives of
+ * one communicator running at the same time would share it.  Different
+ * communicators are independent.  ccl_last_error() is per host thread.
  */
 #ifndef CCL_H
 #define CCL_H

@@ -186,6 +186,7 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
     a.status = L.status;
     a.wait_ns = L.wait_limit_ns;
     a.stall_test = 0;
+    a.dynamic = 0;
 
     auto kern = bulkred_kernel<T, OP, P>;
     static std::atomic<bool> attr{false};  // set once; racing first calls both set it

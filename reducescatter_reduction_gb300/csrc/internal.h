@@ -64,7 +64,7 @@ struct LaunchInfo {
 // least two stages fit.  want_tile != 0 forces T.  False if no geometry fits.
 constexpr size_t kTmaSmemLimit = 227 * 1024;
 constexpr int kTmaMaxStages = 8;
-constexpr size_t kTmaCtlBytes = 64;
+constexpr size_t kTmaCtlBytes = 128;
 
 inline bool tma_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stages, size_t *smem)
 {

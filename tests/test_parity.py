@@ -520,9 +520,9 @@ def test_dependent_launch_chain(graph):
         ag = ccl.ccl_comm_create(p, d.ptrs())
         try:
             def chain(s):
+                assert torch.cuda.current_stream().cuda_stream == s
                 ccl.ccl_allreduce(cm_ab.h, "sum", "f32", n, "ring", s)
-                with torch.cuda.stream(torch.cuda.ExternalStream(s)):
-                    b.views[0].view(torch.float32).mul_(2.0)
+                b.views[0].view(torch.float32).mul_(2.0)            # torch's current stream is s
                 ccl.ccl_allreduce(cm_bc.h, "max", "f32", n, "allpairs", s)
                 ccl.ccl_allreduce(cm_cb.h, "sum", "f32", n, "ring", s)
                 ccl.ccl_reduce_scatter(cm_bd.h, "sum", "f32", n, "ring", s)

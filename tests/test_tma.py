@@ -81,6 +81,32 @@ def test_tma_in_place_and_budgets_equal_ldst(p):
         assert ins.guards_intact()
 
 
+def test_tma_tile_counter_starts_at_zero_for_every_launch():
+    """On messages with many tiles per CTA the TMA kernel hands out tiles
+    from a counter in the communicator's status block, and the last CTA of a
+    launch returns it to zero.  Four launches in a row on one stream (counter
+    on 3 SMs, on 2 SMs, the static split on every SM, the counter on 3 SMs
+    again), each after its outputs were zeroed on the same stream and with no
+    host synchronisation in between: a launch that started from a stale
+    counter would leave zero tiles behind."""
+    p, n = 8, 8 * (3 * 8192 + 40)                  # ragged last tile in every chunk
+    xs = gen("f32", "sum", p, n, seed=47)
+    ref, _ = run_collective(xs, "ar", "sum", "f32", "ring", variant="ldst")
+    ins = RankBuffers(xs, n, np.float32)
+    outs = RankBuffers(None, n, np.float32, p=p)
+    with Comm(ins, outs) as cm:
+        for budget, tile in ((3, 2048), (2, 1024), (0, 0), (3, 2048)):
+            for v in outs.views:
+                v.zero_()
+            ccl.ccl_set_launch(cm.h, budget, "tma", tile)
+            ccl.ccl_allreduce(cm.h, "sum", "f32", n, "ring", stream_ptr())
+        torch.cuda.synchronize()
+        ccl.ccl_comm_check(cm.h)
+    for r in range(p):
+        assert torch.equal(outs.views[r], ref.views[0]), r
+    assert outs.guards_intact()
+
+
 def test_tma_statuses():
     p = 4
     xs = gen("bf16", "sum", p, 4 * 1001, seed=43)          # chunk 1001 elements: not 16-byte aligned
