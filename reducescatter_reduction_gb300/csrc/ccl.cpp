@@ -514,8 +514,8 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
         const bool fits = variant == CCL_VARIANT_TMA ? tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem)
                                                      : bulkred_geometry(p, c->pipe_bytes, &tile, &stages, &smem);
         if (!fits)
-            return fail(CCL_ERR_INVALID_ARG, "pipeline_chunk_bytes %zu: fewer than 2 stages of %d+1 tiles fit in shared memory",
-                        c->pipe_bytes, p);
+            return fail(CCL_ERR_INVALID_ARG, "pipeline_chunk_bytes %zu: fewer than 2 stages of %d tiles fit in shared memory",
+                        c->pipe_bytes, variant == CCL_VARIANT_TMA ? p + 1 : p);
     }
 
     LaunchInfo info;
