@@ -9,7 +9,6 @@ import pytest
 import torch
 
 import oracle
-import reducescatter_reduction_gb300 as ccl
 from reducescatter_reduction_gb300 import inputs
 from ccl_testutil import bits_equal, ensure_built
 from test_parity import gen, run_collective
