@@ -195,8 +195,11 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
         total = 0.0f;
         for (int k = 0; k < C; ++k) total = __fadd_rn(total, *cluster.map_shared_rank(&slice_sum, k));
         // No CTA may leave while another may still read its sum: arrive
-        // now, wait at the end, so the wait overlaps pass 2.
-        cluster.barrier_arrive();
+        // now, wait at the end, so the wait overlaps pass 2.  The arrival
+        // publishes nothing, so it is relaxed (3.32 vs 3.59 us per decode
+        // call); taking `total` as an operand keeps every remote read --
+        // each one consumed by an add into total -- ahead of it.
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::"f"(total) : "memory");
     }
     const float inv = 1.0f / sqrtf(__fadd_rn(__fdiv_rn(total, float(H)), a.eps));
 
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
             for (int k = 0; k < p; ++k) Tr::store1(a.dst[k], e, o);
         }
     }
-    if (C > 1) cluster.barrier_wait();
+    if (C > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 template <typename T, int P>
