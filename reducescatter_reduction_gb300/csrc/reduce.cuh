@@ -255,6 +255,7 @@ static cudaError_t launch_op_mode(const Launch &L, LaunchInfo *info)
 {
     switch (L.p) {
     case 2: return launch_p<T, OP, 2, MODE>(L, info);
+    case 3: return launch_p<T, OP, 3, MODE>(L, info);
     case 4: return launch_p<T, OP, 4, MODE>(L, info);
     case 8: return launch_p<T, OP, 8, MODE>(L, info);
     case 16: return launch_p<T, OP, 16, MODE>(L, info);
