@@ -259,7 +259,9 @@ CCL_API ccl_status_t ccl_allreduce_residual_rmsnorm(ccl_comm_t comm, ccl_dtype_t
  * cudaFree, no allocating library routine.
  *
  * Computes exactly what ccl_allreduce computes (same chunks, same orders, same
- * bits) with the TMA variant's kernel: out_ptrs[r][e] = reduction over k of
+ * bits) with the TMA variant's kernel and its static tile split (no tile
+ * counter, so nothing but the status record is shared between calls):
+ * out_ptrs[r][e] = reduction over k of
  * in_ptrs[k][e], e < n, for every r.  p in [1, 64]; in_ptrs / out_ptrs are host
  * arrays of p device pointers (in place: out_ptrs[r] == in_ptrs[r]; any other
  * overlap is CCL_ERR_INVALID_ARG); schedule is AUTO (cost model, no

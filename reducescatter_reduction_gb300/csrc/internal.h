@@ -43,6 +43,7 @@ struct Launch {
     int sm_budget = 0;         // 0 = all SMs
     size_t pipe_bytes = 0;     // TMA stage bytes per rank
     unsigned *status = nullptr;  // device status block
+    bool tile_counter = true;  // TMA: large messages may take tiles from a counter in the status block
     long long wait_limit_ns = 0;
     int stall_test = 0;
     cudaStream_t stream = nullptr;

@@ -10,9 +10,10 @@
 // API allocates a small status block per communicator; this entry point
 // allocates nothing.
 //
-// What it runs: the TMA variant's AllReduce kernel (tma.cuh), unchanged.  That
-// kernel's only memory beyond the caller's inputs and outputs is the status
-// record its bounded waits write when one gives up.  Here the record lives in
+// What it runs: the TMA variant's AllReduce kernel (tma.cuh) with its static
+// tile split (no tile counter).  That kernel's only memory beyond the
+// caller's inputs and outputs is then the status record its bounded waits
+// write when one gives up.  Here the record lives in
 // a file-scope device array of this library, kStaticScratchBytes long, which
 // every GPU that loads the library holds until the process exits.
 #include <cuda_runtime.h>
@@ -174,6 +175,7 @@ extern "C" ccl_status_t ccl_allreduce_static(int p, void *const *in_ptrs, void *
     L.sm_budget = 0;
     L.pipe_bytes = 0;
     L.status = static_cast<unsigned *>(scratch);
+    L.tile_counter = false;  // the static split: nothing shared between calls but the status record
     L.wait_limit_ns = 2000000000LL;
     L.stall_test = 0;
     L.stream = st;

@@ -409,7 +409,7 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) cap = uint64_t(L.sm_budget);
     const int grid = int(tiles < cap ? (tiles ? tiles : 1) : cap);
     // the tile counter pays off once every CTA has many grabs to balance
-    a.dynamic = tiles >= 16ull * kTmaGrab * uint64_t(grid) ? 1 : 0;
+    a.dynamic = L.tile_counter && tiles >= 16ull * kTmaGrab * uint64_t(grid) ? 1 : 0;
     kern<<<grid, kTmaThreads, smem, L.stream>>>(a);
     if (info) {
         info->kernel = MODE == MODE_AR ? "allreduce_tma" : "reduce_scatter_tma";
