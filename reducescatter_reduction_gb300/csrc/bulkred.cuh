@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
         fence_proxy_async_smem();
     }
     __syncthreads();
+    grid_dependency_wait();  // launched as a dependent: no global access before this
 
     const uint64_t ntiles = a.tstart[p];
     const uint64_t first = uint64_t(blockIdx.x) * K + j, step = uint64_t(gridDim.x) * K;
@@ -217,7 +218,8 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
     const uint64_t ctas = (tiles + pipes - 1) / pipes;
     const int grid = int(ctas < cap ? (ctas ? ctas : 1) : cap);
     const int block = int(pipes) * kBulkThreads;
-    kern<<<grid, block, smem, L.stream>>>(a);
+    cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(block), smem, L.stream, a);
+    if (err != cudaSuccess) return err;
     if (info) {
         info->kernel = MODE_AR == L.mode ? "allreduce_tma_bulkred" : "reduce_scatter_tma_bulkred";
         info->grid = grid;

@@ -224,6 +224,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         fence_proxy_async_smem();
     }
     __syncthreads();
+    // Launched as a dependent: the set-up above overlaps the previous
+    // kernel's tail; no global memory is touched before this wait.
+    grid_dependency_wait();
 
     const uint64_t ntiles = a.tstart[p];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -410,7 +413,8 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
     const int grid = int(tiles < cap ? (tiles ? tiles : 1) : cap);
     // the tile counter pays off once every CTA has many grabs to balance
     a.dynamic = L.tile_counter && tiles >= 16ull * kTmaGrab * uint64_t(grid) ? 1 : 0;
-    kern<<<grid, kTmaThreads, smem, L.stream>>>(a);
+    cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(kTmaThreads), smem, L.stream, a);
+    if (err != cudaSuccess) return err;
     if (info) {
         info->kernel = MODE == MODE_AR ? "allreduce_tma" : "reduce_scatter_tma";
         info->grid = grid;
