@@ -87,7 +87,8 @@ def test_tp_activation_fused_rmsnorm(dtype, tokens):
 @pytest.mark.parametrize("p,rows,hidden,sched", [(3, 5, 1000, "allpairs"), (8, 7, 1023, "ring"),
                                                  (16, 2, 4096, "allpairs"), (2, 9, 64, "ring"),
                                                  (8, 200, 1023, "ring"), (8, 160, 12288, "allpairs"),
-                                                 (3, 400, 1000, "allpairs"), (8, 350, 9216, "ring")])
+                                                 (3, 400, 1000, "allpairs"), (8, 350, 9216, "ring"),
+                                                 (1, 7, 1000, "ring"), (1, 300, 8192, "allpairs")])
 def test_fused_rmsnorm_shapes_and_in_place(dtype, p, rows, hidden, sched):
     """Rows below, between one and two times, and above twice the SM count
     take the three CTA shapes (128-thread clusters, 1024-thread CTAs,
