@@ -160,11 +160,13 @@ CCL_API ccl_status_t ccl_comm_set_outputs(ccl_comm_t comm, void *const *out_ptrs
 CCL_API ccl_status_t ccl_comm_set_schedule(ccl_comm_t comm, const uint8_t *order);
 
 /* Launch shape.
- *  sm_budget : 0 = all SMs; k > 0 = at most k CTAs, one per SM (persistent),
- *              the restricted-CTA-budget setting of T-CCL, section
- *              "Collective Operation Performance" (Fig. 4, Table IV).  Larger
- *              than the SM count = all SMs.  The comparison executors and
- *              ccl_allreduce_residual_rmsnorm always use every SM.
+ *  sm_budget : 0 = all SMs; k > 0 = at most k CTAs, so at most k SMs, the
+ *              restricted-CTA-budget setting of T-CCL, section "Collective
+ *              Operation Performance" (Fig. 4, Table IV).  Messages that need
+ *              more than k CTAs of the regular kernel run one persistent,
+ *              large CTA per SM.  Larger than the SM count = all SMs.  The
+ *              comparison executors and ccl_allreduce_residual_rmsnorm always
+ *              use every SM.
  *  variant   : a ccl_variant_t.
  *  pipeline_chunk_bytes : 0 = the variant's default.  For the TMA variants,
  *              the bytes per rank moved per pipeline stage (multiple of 16,
