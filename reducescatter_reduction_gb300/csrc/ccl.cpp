@@ -511,8 +511,11 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
                         "the TMA variant needs 16-byte aligned pointers and chunk boundaries (n=%zu, p=%d)", n, p);
         uint32_t tile, stages;
         size_t smem;
-        const bool fits = variant == CCL_VARIANT_TMA ? tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem)
-                                                     : bulkred_geometry(p, c->pipe_bytes, &tile, &stages, &smem);
+        uint32_t ranks;
+        const bool fits = variant == CCL_VARIANT_TMA
+                              ? (p > kTmaNarrowMaxRanks ? tma_wide_geometry(p, c->pipe_bytes, &tile, &ranks, &stages, &smem)
+                                                        : tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem))
+                              : bulkred_geometry(p, c->pipe_bytes, &tile, &stages, &smem);
         if (!fits)
             return fail(CCL_ERR_INVALID_ARG, "pipeline_chunk_bytes %zu: fewer than 2 stages of %d tiles fit in shared memory",
                         c->pipe_bytes, variant == CCL_VARIANT_TMA ? p + 1 : p);

@@ -85,6 +85,32 @@ inline bool tma_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stag
     return false;
 }
 
+// Above kTmaNarrowMaxRanks ranks a stage holding one tile of every rank
+// would force 1 KB tiles (p+1 of them per stage), and 1 KB bulk copies cost
+// more per byte.  The wide geometry keeps T bytes per copy and brings the p
+// ranks through the stages R at a time (a tile takes ceil(p/R) stages); two
+// output tiles sit beside the stages.  T <= 8 KB so that each consumer
+// thread folds at most two 16-byte groups per tile in registers.
+constexpr int kTmaNarrowMaxRanks = 32;
+constexpr int kTmaWideRanks = 8;          // R: ranks per stage
+
+inline bool tma_wide_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *ranks, uint32_t *stages,
+                              size_t *smem)
+{
+    const size_t T = want_tile ? want_tile : 8192;
+    if (T > 8192 || T < 1024) return false;
+    const size_t R = size_t(p) < size_t(kTmaWideRanks) ? size_t(p) : size_t(kTmaWideRanks);
+    const size_t fixed = 2 * T + 2 * kTmaMaxStages * 8 + kTmaCtlBytes;
+    size_t S = (kTmaSmemLimit - fixed) / (R * T);
+    if (S > size_t(kTmaMaxStages)) S = kTmaMaxStages;
+    if (S < 2) return false;
+    *tile = uint32_t(T);
+    *ranks = uint32_t(R);
+    *stages = uint32_t(S);
+    *smem = S * R * T + 2 * T + 2 * S * 8 + kTmaCtlBytes;
+    return true;
+}
+
 // Bulk-reduce variant: the reductions the PTX bulk-reduce instruction
 // provides (sum on f32/f16/bf16/i32, min/max on f16/bf16/i32), and its
 // geometry: two stages of p tiles, small enough for several CTAs per SM.

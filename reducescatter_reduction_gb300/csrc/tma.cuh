@@ -54,6 +54,7 @@ struct TmaArgs {
     long long wait_ns;          // bound on any single wait
     int stall_test;             // 1: the producer withholds its second tile (timeout test)
     int dynamic;                // 1: tiles beyond each CTA's first grab come from the tile counter
+    uint32_t ranks_per_stage;   // wide kernel: R ranks of a tile per stage
 };
 
 // ---------------------------------------------------------------------------
@@ -365,6 +366,193 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Wide variant (p > kTmaNarrowMaxRanks): a tile's p ranks pass through the
+// stages R at a time.  The producer loads ranks order[c][b*R ...] of tile t
+// into a stage (one stage per batch b = 0 .. B-1, B = ceil(p/R)); each
+// consumer thread keeps the fp32 partial of its 16-byte groups of the tile
+// in registers across the B batches, folding in the chunk's order exactly as
+// the narrow kernel does, and after the last batch writes the tile to one of
+// two output tiles, from which one thread issues the bulk fan-out stores.
+// Waits, abort, drain and the tile counter work as in the narrow kernel (one
+// tile per visit: a tile is B stages of work).
+// ---------------------------------------------------------------------------
+
+constexpr int kTmaWideGroups = 2;  // 16-byte groups per consumer thread per tile (T <= 8 KB)
+
+template <typename T, int OP, int MODE>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    tma_wide_kernel(const __grid_constant__ TmaArgs<kMaxRanks> a)
+{
+    using Tr = Traits<T>;
+    using F = Fold<T, OP>;
+    using Acc = typename Tr::Acc;
+    constexpr int VEC = Tr::VEC;
+    constexpr int S_ELEM = (VEC == 8) ? 2 : 4;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int p = a.p;
+    const uint32_t TB = a.tile_bytes, S = a.stages, R = a.ranks_per_stage;
+    const uint32_t B = (uint32_t(p) + R - 1) / R;                    // stages per tile
+    unsigned char *in_base = smem;                                   // [S][R][TB]
+    unsigned char *out_base = smem + size_t(S) * R * TB;             // [2][TB]
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_base + 2 * size_t(TB));
+    uint64_t *empty = full + S;
+    volatile TmaCtl *ctl = reinterpret_cast<volatile TmaCtl *>(empty + S);
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < S; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), kTmaConsumerWarps);
+        }
+        ctl->abort = 0;
+        ctl->go = 0;
+        ctl->issued = 0;
+        ctl->consumed = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    grid_dependency_wait();  // launched as a dependent: no global access before this
+
+    const uint64_t ntiles = a.tstart[p];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            // Each CTA's first tile is blockIdx.x; the rest come from the
+            // tile counter (large messages) or a static stride.
+            unsigned long long *next = reinterpret_cast<unsigned long long *>(a.status + 4);
+            int c = 0;
+            uint32_t i = 0;
+            bool stopped = false;
+            for (uint64_t t = blockIdx.x; t < ntiles && !stopped;
+                 t = a.dynamic ? gridDim.x + atomicAdd(next, 1ull) : t + gridDim.x) {
+                while (t >= a.tstart[c + 1]) ++c;
+                const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
+                const uint64_t off = cb + (t - a.tstart[c]) * TB;
+                const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
+                for (uint32_t b = 0; b < B; ++b, ++i) {
+                    const uint32_t s = i % S;
+                    if (i >= S && !bounded_wait(a, ctl, smem_addr(&empty[s]), ((i / S) - 1) & 1u, 2u, i)) {
+                        stopped = true;
+                        break;
+                    }
+                    if (a.stall_test && i == 1) {  // withhold this stage: its consumers must time out
+                        stopped = true;
+                        break;
+                    }
+                    const uint32_t nb = uint32_t(p) - b * R < R ? uint32_t(p) - b * R : R;
+                    ctl->tile_of[s] = (t << 8) | b;
+                    const uint32_t bar = smem_addr(&full[s]);
+                    mbar_arrive_expect_tx(bar, nb * bytes);
+                    unsigned char *slot = in_base + size_t(s) * R * TB;
+                    for (uint32_t j = 0; j < nb; ++j)
+                        bulk_load(smem_addr(slot + size_t(j) * TB),
+                                  static_cast<const char *>(a.src[a.order[c][b * R + j]]) + off, bytes, bar);
+                    ctl->issued = i + 1;
+                }
+            }
+            if (!stopped) {
+                // no more work: a stage with no bytes wakes the consumers
+                const uint32_t s = i % S;
+                if (i < S || bounded_wait(a, ctl, smem_addr(&empty[s]), ((i / S) - 1) & 1u, 2u, i)) {
+                    ctl->tile_of[s] = kNoTile;
+                    mbar_arrive(smem_addr(&full[s]));
+                }
+            }
+        }
+    } else {
+        // ------------------------------ consumers -----------------------------
+        const int tid = threadIdx.x - 32;
+        Acc acc[kTmaWideGroups][VEC];
+        int c = 0;
+        uint32_t k = 0;  // tiles finished (output tile k & 1)
+        for (uint32_t i = 0;; ++i) {
+            const uint32_t s = i % S;
+            if (tid == 0) ctl->go = bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, i) ? 1 : 0;
+            consumer_barrier();
+            if (!ctl->go) break;
+            const unsigned long long meta = ctl->tile_of[s];
+            if (meta == kNoTile) break;
+            const uint64_t t = meta >> 8;
+            const uint32_t b = uint32_t(meta & 255u);
+            while (t >= a.tstart[c + 1]) ++c;
+            const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
+            const uint64_t off = cb + (t - a.tstart[c]) * TB;
+            const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
+            const uint32_t nb = uint32_t(p) - b * R < R ? uint32_t(p) - b * R : R;
+            const uint32_t in_s = smem_addr(in_base + size_t(s) * R * TB);
+#pragma unroll
+            for (int q = 0; q < kTmaWideGroups; ++q) {
+                const uint32_t g = uint32_t(tid) + uint32_t(q) * kTmaConsumers;
+                if (g * 16 >= bytes) continue;
+                Acc v[VEC];
+                for (uint32_t j = 0; j < nb; ++j) {
+                    Tr::unpack(lds_v4(in_s + j * TB + g * 16), v);
+                    if (b == 0 && j == 0) {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc[q][e] = F::first(v[e], a.scale);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc[q][e] = F::fold(acc[q][e], v[e], a.scale);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&empty[s]));  // this stage's input slots are free
+            if (tid == 0) ctl->consumed = i + 1;
+            if (b + 1 == B) {
+                // the tile is complete: write it to output tile k & 1, whose
+                // stores from tile k - 2 must have finished reading it
+                const uint32_t out_s = smem_addr(out_base + size_t(k & 1u) * TB);
+                if (tid == 0 && k >= 2) bulk_wait_read(1);
+                consumer_barrier();
+#pragma unroll
+                for (int q = 0; q < kTmaWideGroups; ++q) {
+                    const uint32_t g = uint32_t(tid) + uint32_t(q) * kTmaConsumers;
+                    if (g * 16 >= bytes) continue;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[q][e] = F::finish(acc[q][e], p);
+                    sts_v4(out_s + g * 16, Tr::pack(acc[q]));
+                }
+                fence_proxy_async_smem();                      // out tile visible to the bulk stores
+                consumer_barrier();
+                if (tid == 0) {
+                    if constexpr (MODE == MODE_AR) {
+                        for (int r = 0; r < p; ++r) bulk_store(static_cast<char *>(a.dst[r]) + off, out_s, bytes);
+                    } else {
+                        bulk_store(static_cast<char *>(a.dst[c]) + (off - cb), out_s, bytes);
+                    }
+                    bulk_commit();
+                }
+                ++k;
+            }
+        }
+        if (tid == 0) bulk_wait_all();
+    }
+    __syncthreads();
+    // After an abort, wait (bounded) for loads still in flight into shared
+    // memory before the CTA gives its shared memory back.
+    if (threadIdx.x == 0 && ctl->abort) {
+        const uint32_t issued = ctl->issued;
+        for (uint32_t j = ctl->consumed; j < issued; ++j) {
+            const uint32_t bar = smem_addr(&full[j % S]);
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(bar, (j / S) & 1u))
+                if (global_ns() - t0 > uint64_t(a.wait_ns)) break;
+        }
+    }
+    // the last CTA to finish returns the tile counter to zero
+    if (a.dynamic && threadIdx.x == 0) {
+        if (atomicAdd(a.status + 6, 1u) == gridDim.x - 1) {
+            atomicExch(reinterpret_cast<unsigned long long *>(a.status + 4), 0ull);
+            atomicExch(a.status + 6, 0u);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
 
@@ -426,6 +614,58 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
 }
 
 template <typename T, int OP, int MODE>
+static cudaError_t tma_wide_launch(const Launch &L, LaunchInfo *info)
+{
+    constexpr int S_ELEM = (Traits<T>::VEC == 8) ? 2 : 4;
+    TmaArgs<kMaxRanks> a;
+    uint32_t tile = 0, ranks = 0, stages = 0;
+    size_t smem = 0;
+    if (!tma_wide_geometry(L.p, L.pipe_bytes, &tile, &ranks, &stages, &smem)) return cudaErrorInvalidValue;
+    for (int k = 0; k < L.p; ++k) {
+        a.src[k] = L.src[k];
+        a.dst[k] = L.dst[k];
+    }
+    uint64_t tiles = 0;
+    for (int c = 0; c <= L.p; ++c) {
+        a.bound[c] = L.table->bound[c];
+        a.tstart[c] = tiles;
+        if (c < L.p) tiles += ((L.table->bound[c + 1] - L.table->bound[c]) * S_ELEM + tile - 1) / tile;
+    }
+    for (int c = 0; c < L.p; ++c)
+        for (int k = 0; k < L.p; ++k) a.order[c][k] = L.table->order[c * L.p + k];
+    a.p = L.p;
+    a.scale = 1.0f / float(L.p);
+    a.tile_bytes = tile;
+    a.stages = stages;
+    a.ranks_per_stage = ranks;
+    a.status = L.status;
+    a.wait_ns = L.wait_limit_ns;
+    a.stall_test = L.stall_test;
+
+    auto kern = tma_wide_kernel<T, OP, MODE>;
+    static std::atomic<bool> attr{false};  // set once; racing first calls both set it
+    if (!attr.load(std::memory_order_acquire)) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTmaSmemLimit));
+        if (err != cudaSuccess) return err;
+        attr.store(true, std::memory_order_release);
+    }
+    uint64_t cap = uint64_t(L.num_sms);
+    if (L.sm_budget > 0 && L.sm_budget < L.num_sms) cap = uint64_t(L.sm_budget);
+    const int grid = int(tiles < cap ? (tiles ? tiles : 1) : cap);
+    a.dynamic = L.tile_counter && tiles >= 16ull * uint64_t(grid) ? 1 : 0;  // a tile here is B stages of work
+    cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(kTmaThreads), smem, L.stream, a);
+    if (err != cudaSuccess) return err;
+    if (info) {
+        info->kernel = MODE == MODE_AR ? "allreduce_tma_wide" : "reduce_scatter_tma_wide";
+        info->grid = grid;
+        info->block = kTmaThreads;
+        info->smem = smem;
+        info->kernels = 1;
+    }
+    return cudaGetLastError();
+}
+
+template <typename T, int OP, int MODE>
 static cudaError_t tma_launch_op_mode(const Launch &L, LaunchInfo *info)
 {
     switch (L.p) {
@@ -433,7 +673,9 @@ static cudaError_t tma_launch_op_mode(const Launch &L, LaunchInfo *info)
     case 4: return tma_launch_p<T, OP, 4, MODE>(L, info);
     case 8: return tma_launch_p<T, OP, 8, MODE>(L, info);
     case 16: return tma_launch_p<T, OP, 16, MODE>(L, info);
-    default: return tma_launch_p<T, OP, 0, MODE>(L, info);
+    default:
+        return L.p > kTmaNarrowMaxRanks ? tma_wide_launch<T, OP, MODE>(L, info)
+                                        : tma_launch_p<T, OP, 0, MODE>(L, info);
     }
 }
 

@@ -107,6 +107,62 @@ def test_tma_tile_counter_starts_at_zero_for_every_launch():
     assert outs.guards_intact()
 
 
+@pytest.mark.parametrize("dtype,op", [("bf16", "sum"), ("f32", "avg"), ("i32", "prod"), ("f16", "max")])
+def test_tma_wide_ranks_match_oracle(dtype, op):
+    """More than 32 ranks: the wide kernel brings a tile's ranks through the
+    stages eight at a time and keeps the partial in registers across them;
+    bits equal the oracle for AllReduce and ReduceScatter, with a short last
+    tile, a last batch of fewer than eight ranks, several tile sizes and an
+    SM budget."""
+    s = inputs.ELEM_BYTES[dtype]
+    per16 = 16 // s
+    for p, tile, budget in ((33, 0, 0), (40, 4096, 3), (64, 1024, 0), (64, 0, 7)):
+        n = p * (3 * 8192 // s + 5 * per16)
+        xs = gen(dtype, op, p, n, seed=150 + p)
+        storage = inputs.STORAGE[dtype]
+        ins = RankBuffers(xs, n, storage)
+        outs = RankBuffers(None, n, storage, p=p)
+        with Comm(ins, outs) as cm:
+            ccl.ccl_set_launch(cm.h, budget, "tma", tile)
+            ccl.ccl_allreduce(cm.h, op, dtype, n, "ring", stream_ptr())
+            torch.cuda.synchronize()
+            desc = ccl.ccl_comm_last_launch(cm.h)
+            ccl.ccl_comm_check(cm.h)
+        assert "allreduce_tma_wide" in desc, desc
+        if budget:
+            assert int(desc.split("grid=")[1].split()[0]) <= budget
+        want = oracle.allreduce(xs, op, dtype, "ring")
+        for r in range(p):
+            assert bits_equal(outs.host(r), want[r]), (p, tile, budget, r)
+        assert ins.guards_intact() and outs.guards_intact()
+        rs, desc = run_collective(xs, "rs", op, dtype, "allpairs", variant="tma")
+        assert "reduce_scatter_tma_wide" in desc
+        want = oracle.reduce_scatter(xs, op, dtype, "allpairs")
+        for r in range(p):
+            assert bits_equal(rs.host(r), want[r]), (p, r)
+
+
+def test_tma_wide_bounded_wait_times_out_and_context_survives():
+    p, n = 40, 40 * (1 << 13)
+    xs = gen("bf16", "sum", p, n, seed=160)
+    storage = inputs.STORAGE["bf16"]
+    ins = RankBuffers(xs, n, storage)
+    outs = RankBuffers(None, n, storage, p=p)
+    with Comm(ins, outs) as cm:
+        ccl.ccl_set_launch(cm.h, 1, "tma", 2048)
+        ccl.ccl_comm_set_debug(cm.h, 20_000_000, 1)
+        ccl.ccl_allreduce(cm.h, "sum", "bf16", n, "ring", stream_ptr())
+        with pytest.raises(ccl.CclError) as ei:
+            ccl.ccl_comm_check(cm.h)
+        assert ei.value.status == ccl.CCL_ERR_TIMEOUT
+        ccl.ccl_comm_set_debug(cm.h, 0, 0)
+        ccl.ccl_allreduce(cm.h, "sum", "bf16", n, "ring", stream_ptr())
+        ccl.ccl_comm_check(cm.h)
+    want = oracle.allreduce(xs, "sum", "bf16", "ring")
+    for r in range(p):
+        assert bits_equal(outs.host(r), want[r])
+
+
 def test_tma_statuses():
     p = 4
     xs = gen("bf16", "sum", p, 4 * 1001, seed=43)          # chunk 1001 elements: not 16-byte aligned
