@@ -6,8 +6,9 @@
 // TMA unit; a D-stage shared-memory pipeline keeps some stages loading while
 // others are being stored, each stage waiting for its load to complete before
 // its store is issued, and for its previous store before it is reloaded.
-// Here one CTA per SM (persistent; or k CTAs under an SM budget) takes tiles
-// from a device-wide counter, a few at a time, until none are left; a tile
+// Here one CTA per SM (persistent; or k CTAs under an SM budget) walks the
+// tiles -- on large messages taking them from a device-wide counter, a few
+// at a time, until none are left; on small ones by a static stride.  A tile
 // is T bytes of one chunk, taken from every rank:
 //
 //   producer (warp 0, one lane):  wait stage free -> expect p*T bytes ->
@@ -28,7 +29,9 @@
 // boundary and pointer is 16-byte aligned).  The counter lives in the
 // communicator's status block and the last CTA of a launch returns it to
 // zero, so launches on one status block must be ordered (one stream, or
-// synchronised), as every collective on one communicator already is.
+// synchronised), as every collective on one communicator already is.  Above
+// 32 ranks the wide kernel further down takes over (ranks through the stages
+// eight at a time).
 #pragma once
 
 #include "device.cuh"
