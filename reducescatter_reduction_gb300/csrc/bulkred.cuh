@@ -71,7 +71,10 @@ template <typename T, int OP> struct BulkRed {
 // region and its own tiles (pipe j of CTA b takes tiles b*K + j, stepping by
 // gridDim.x*K).  The issuing lane's wait for each tile's first store to land
 // serialises one pipe; several pipes per CTA keep several tiles' reductions in
-// flight on one SM, which is what an SM budget (one CTA per SM) needs.
+// flight on one SM, which is what an SM budget (one CTA per SM) needs.  A
+// stage holds R ranks of a tile; above 16 ranks R < p and a tile takes
+// ceil(p/R) stages, the first storing its first rank and every later one only
+// reducing into the tile's destination.
 template <typename T, int OP, int P>
 __global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
     bulkred_kernel(const __grid_constant__ TmaArgs<(P > 0 ? P : kMaxRanks)> a)
@@ -79,11 +82,12 @@ __global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
     constexpr int S_ELEM = (Traits<T>::VEC == 8) ? 2 : 4;
     extern __shared__ __align__(128) unsigned char smem[];
     const int p = P > 0 ? P : a.p;
-    const uint32_t TB = a.tile_bytes, S = a.stages;
+    const uint32_t TB = a.tile_bytes, S = a.stages, R = a.ranks_per_stage;
+    const uint32_t NB = (uint32_t(p) + R - 1) / R;   // stages per tile
     const uint32_t K = blockDim.x / kBulkThreads, j = threadIdx.x / kBulkThreads;
     const uint32_t lt = threadIdx.x % kBulkThreads;
-    unsigned char *in_base = smem + size_t(j) * bulkred_pipe_bytes(p, TB, S);   // [S][p][TB]
-    uint64_t *full = reinterpret_cast<uint64_t *>(in_base + size_t(S) * p * TB);
+    unsigned char *in_base = smem + size_t(j) * bulkred_pipe_bytes(int(R), TB, S);   // [S][R][TB]
+    uint64_t *full = reinterpret_cast<uint64_t *>(in_base + size_t(S) * R * TB);
     uint64_t *empty = full + S;
     volatile TmaCtl *ctl = reinterpret_cast<volatile TmaCtl *>(empty + S);
 
@@ -107,42 +111,60 @@ __global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
         // producer
         int c = 0;
         uint32_t i = 0;
-        for (uint64_t t = first; t < ntiles; t += step, ++i) {
-            const uint32_t s = i % S;
-            if (i >= S && !bounded_wait(a, ctl, smem_addr(&empty[s]), ((i / S) - 1) & 1u, 2u, t)) break;
+        bool stopped = false;
+        for (uint64_t t = first; t < ntiles && !stopped; t += step) {
             while (t >= a.tstart[c + 1]) ++c;
             const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
             const uint64_t off = cb + (t - a.tstart[c]) * TB;
             const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
-            const uint32_t bar = smem_addr(&full[s]);
-            mbar_arrive_expect_tx(bar, uint32_t(p) * bytes);
-            unsigned char *slot = in_base + size_t(s) * p * TB;
-            for (int k = 0; k < p; ++k)
-                bulk_load(smem_addr(slot + size_t(k) * TB), static_cast<const char *>(a.src[a.order[c][k]]) + off,
-                          bytes, bar);
-            ctl->issued = i + 1;
+            for (uint32_t b = 0; b < NB; ++b, ++i) {
+                const uint32_t s = i % S;
+                if (i >= S && !bounded_wait(a, ctl, smem_addr(&empty[s]), ((i / S) - 1) & 1u, 2u, t)) {
+                    stopped = true;
+                    break;
+                }
+                const uint32_t nb = uint32_t(p) - b * R < R ? uint32_t(p) - b * R : R;
+                const uint32_t bar = smem_addr(&full[s]);
+                mbar_arrive_expect_tx(bar, nb * bytes);
+                unsigned char *slot = in_base + size_t(s) * R * TB;
+                for (uint32_t k = 0; k < nb; ++k)
+                    bulk_load(smem_addr(slot + size_t(k) * TB),
+                              static_cast<const char *>(a.src[a.order[c][b * R + k]]) + off, bytes, bar);
+                ctl->issued = i + 1;
+            }
         }
     } else if (lt == 32) {
         // issuer
         int c = 0;
         uint32_t i = 0;
-        for (uint64_t t = first; t < ntiles; t += step, ++i) {
-            const uint32_t s = i % S;
-            if (!bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, t)) break;
+        bool stopped = false;
+        for (uint64_t t = first; t < ntiles && !stopped; t += step) {
             while (t >= a.tstart[c + 1]) ++c;
             const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
             const uint64_t off = cb + (t - a.tstart[c]) * TB;
             const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
-            const uint32_t slot = smem_addr(in_base + size_t(s) * p * TB);
             char *dst = static_cast<char *>(a.dst[c]) + (off - cb);
-            bulk_store(dst, slot, bytes);          // the first contribution lands first
-            bulk_commit();
-            bulk_wait_all();
-            for (int k = 1; k < p; ++k) BulkRed<T, OP>::issue(dst, slot + k * TB, bytes);
-            bulk_commit();
-            bulk_wait_read(0);                     // slots read: the stage may be refilled
-            mbar_arrive(smem_addr(&empty[s]));
-            ctl->consumed = i + 1;
+            for (uint32_t b = 0; b < NB; ++b, ++i) {
+                const uint32_t s = i % S;
+                if (!bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, t)) {
+                    stopped = true;
+                    break;
+                }
+                const uint32_t nb = uint32_t(p) - b * R < R ? uint32_t(p) - b * R : R;
+                const uint32_t slot = smem_addr(in_base + size_t(s) * R * TB);
+                uint32_t k0 = 0;
+                if (b == 0) {
+                    bulk_store(dst, slot, bytes);      // the first contribution lands first
+                    bulk_commit();
+                    bulk_wait_all();
+                    k0 = 1;
+                }
+                for (uint32_t k = k0; k < nb; ++k) BulkRed<T, OP>::issue(dst, slot + k * TB, bytes);
+                bulk_commit();
+                bulk_wait_read(0);                     // slots read: the stage may be refilled
+                mbar_arrive(smem_addr(&empty[s]));
+                ctl->consumed = i + 1;
+            }
         }
         bulk_wait_all();
     }
@@ -164,9 +186,9 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
     constexpr int PM = P > 0 ? P : kMaxRanks;
     constexpr int S_ELEM = (Traits<T>::VEC == 8) ? 2 : 4;
     TmaArgs<PM> a;
-    uint32_t tile = 0, stages = 0;
+    uint32_t tile = 0, ranks = 0, stages = 0;
     size_t smem = 0;
-    if (!bulkred_geometry(L.p, L.pipe_bytes, &tile, &stages, &smem)) return cudaErrorInvalidValue;
+    if (!bulkred_geometry(L.p, L.pipe_bytes, &tile, &ranks, &stages, &smem)) return cudaErrorInvalidValue;
     uint64_t tiles = 0;
     for (int c = 0; c <= L.p; ++c) {
         a.bound[c] = L.table->bound[c];
@@ -188,6 +210,7 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
     a.wait_ns = L.wait_limit_ns;
     a.stall_test = 0;
     a.dynamic = 0;
+    a.ranks_per_stage = ranks;
 
     auto kern = bulkred_kernel<T, OP, P>;
     static std::atomic<bool> attr{false};  // set once; racing first calls both set it
@@ -196,7 +219,7 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
         if (err != cudaSuccess) return err;
         attr.store(true, std::memory_order_release);
     }
-    const size_t pipe = bulkred_pipe_bytes(L.p, tile, stages);
+    const size_t pipe = bulkred_pipe_bytes(int(ranks), tile, stages);
     uint64_t cap;
     uint32_t pipes = 1;
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) {

@@ -515,10 +515,11 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
         const bool fits = variant == CCL_VARIANT_TMA
                               ? (p > kTmaNarrowMaxRanks ? tma_wide_geometry(p, c->pipe_bytes, &tile, &ranks, &stages, &smem)
                                                         : tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem))
-                              : bulkred_geometry(p, c->pipe_bytes, &tile, &stages, &smem);
+                              : bulkred_geometry(p, c->pipe_bytes, &tile, &ranks, &stages, &smem);
         if (!fits)
-            return fail(CCL_ERR_INVALID_ARG, "pipeline_chunk_bytes %zu: fewer than 2 stages of %d tiles fit in shared memory",
-                        c->pipe_bytes, variant == CCL_VARIANT_TMA ? p + 1 : p);
+            return fail(CCL_ERR_INVALID_ARG,
+                        "pipeline_chunk_bytes %zu: two pipeline stages of that tile size do not fit in shared memory (p=%d)",
+                        c->pipe_bytes, p);
     }
 
     LaunchInfo info;

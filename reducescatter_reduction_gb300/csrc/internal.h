@@ -121,15 +121,20 @@ inline bool bulkred_supported(int dtype, int op)
     return false;
 }
 
-inline bool bulkred_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stages, size_t *smem)
+inline bool bulkred_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *ranks, uint32_t *stages,
+                             size_t *smem)
 {
-    // default: about 64 KB per CTA, so that three CTAs share an SM
-    size_t T = want_tile ? want_tile : (p <= 4 ? 8192 : p <= 8 ? 4096 : p <= 16 ? 2048 : 1024);
+    // Up to 16 ranks a stage holds a tile of every rank, about 64 KB per
+    // pipe (three pipes per SM).  Above 16 the ranks pass through the stages
+    // eight at a time with 4 KB tiles, instead of shrinking the tiles to 1 KB.
+    const size_t R = p <= 16 ? size_t(p) : 8;
+    size_t T = want_tile ? want_tile : (p <= 4 ? 8192 : p <= 8 ? 4096 : p <= 16 ? 2048 : 4096);
     const uint32_t S = 2;
     for (; T >= 1024; T /= 2) {
-        const size_t bytes = size_t(S) * p * T + 2 * S * 8 + kTmaCtlBytes;
+        const size_t bytes = size_t(S) * R * T + 2 * S * 8 + kTmaCtlBytes;
         if (bytes <= kTmaSmemLimit) {
             *tile = uint32_t(T);
+            *ranks = uint32_t(R);
             *stages = S;
             *smem = bytes;
             return true;

@@ -305,6 +305,28 @@ def test_bulkred_exact_ops_under_budget_match_oracle(budget):
                 assert bits_equal(rs.host(r), want[r]), (dtype, p, r, desc)
 
 
+@pytest.mark.parametrize("p", [17, 24, 40, 64])
+def test_bulkred_many_ranks(p):
+    """Above 16 ranks the bulk-reduce stages hold eight ranks of a tile at a
+    time: int32 sum and bf16 max stay bit-exact, bf16 sum within the bound,
+    with a short last tile and a short last batch, on every SM and under a
+    budget."""
+    for dtype, op in (("i32", "sum"), ("bf16", "max"), ("bf16", "sum")):
+        s = inputs.ELEM_BYTES[dtype]
+        n = p * (3 * 4096 // s + 5 * (16 // s))
+        xs = gen(dtype, op, p, n, seed=170 + p)
+        for budget in (0, 3):
+            res, desc = run_collective(xs, "ar", op, dtype, "ring", variant="tma_bulkred", budget=budget)
+            if op == "sum" and dtype == "bf16":
+                ok, worst = within_reassociation_bound(res.host(0), xs, dtype)
+                assert ok, (p, budget, worst)
+                assert res.identical_across_ranks()
+            else:
+                want = oracle.allreduce(xs, op, dtype, "ring")
+                for r in range(p):
+                    assert bits_equal(res.host(r), want[r]), (dtype, op, p, budget, r, desc)
+
+
 def test_bulkred_reduce_scatter_in_place_and_budget():
     p, dtype = 8, "bf16"
     n = p * (1 << 18)
