@@ -68,8 +68,10 @@ template <typename T, int OP> struct BulkRed {
 // an AllReduce, rank c's output at the chunk's offset.
 //
 // A CTA runs blockDim.x / 64 independent pipes, each on its own shared-memory
-// region and its own tiles (pipe j of CTA b takes tiles b*K + j, stepping by
-// gridDim.x*K).  The issuing lane's wait for each tile's first store to land
+// region and its own tiles (pipe j of CTA b starts at tile b*K + j; further
+// tiles come from the status block's tile counter on large messages, else by
+// a stride of gridDim.x*K; the producer passes each stage's tile and batch to
+// the issuer).  The issuing lane's wait for each tile's first store to land
 // serialises one pipe; several pipes per CTA keep several tiles' reductions in
 // flight on one SM, which is what an SM budget (one CTA per SM) needs.  A
 // stage holds R ranks of a tile; above 16 ranks R < p and a tile takes
@@ -107,12 +109,13 @@ __global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
 
     const uint64_t ntiles = a.tstart[p];
     const uint64_t first = uint64_t(blockIdx.x) * K + j, step = uint64_t(gridDim.x) * K;
+    unsigned long long *next = reinterpret_cast<unsigned long long *>(a.status + 4);
     if (lt == 0) {
-        // producer
+        // producer: first tile static, the rest from the counter (or a stride)
         int c = 0;
         uint32_t i = 0;
         bool stopped = false;
-        for (uint64_t t = first; t < ntiles && !stopped; t += step) {
+        for (uint64_t t = first; t < ntiles && !stopped; t = a.dynamic ? step + atomicAdd(next, 1ull) : t + step) {
             while (t >= a.tstart[c + 1]) ++c;
             const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
             const uint64_t off = cb + (t - a.tstart[c]) * TB;
@@ -124,6 +127,7 @@ __global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
                     break;
                 }
                 const uint32_t nb = uint32_t(p) - b * R < R ? uint32_t(p) - b * R : R;
+                ctl->tile_of[s] = (t << 8) | b;
                 const uint32_t bar = smem_addr(&full[s]);
                 mbar_arrive_expect_tx(bar, nb * bytes);
                 unsigned char *slot = in_base + size_t(s) * R * TB;
@@ -133,38 +137,42 @@ __global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
                 ctl->issued = i + 1;
             }
         }
+        if (!stopped) {
+            const uint32_t s = i % S;
+            if (i < S || bounded_wait(a, ctl, smem_addr(&empty[s]), ((i / S) - 1) & 1u, 2u, i)) {
+                ctl->tile_of[s] = kNoTile;
+                mbar_arrive(smem_addr(&full[s]));
+            }
+        }
     } else if (lt == 32) {
         // issuer
         int c = 0;
-        uint32_t i = 0;
-        bool stopped = false;
-        for (uint64_t t = first; t < ntiles && !stopped; t += step) {
+        for (uint32_t i = 0;; ++i) {
+            const uint32_t s = i % S;
+            if (!bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, i)) break;
+            const unsigned long long meta = ctl->tile_of[s];
+            if (meta == kNoTile) break;
+            const uint64_t t = meta >> 8;
+            const uint32_t b = uint32_t(meta & 255u);
             while (t >= a.tstart[c + 1]) ++c;
             const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
             const uint64_t off = cb + (t - a.tstart[c]) * TB;
             const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
             char *dst = static_cast<char *>(a.dst[c]) + (off - cb);
-            for (uint32_t b = 0; b < NB; ++b, ++i) {
-                const uint32_t s = i % S;
-                if (!bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, t)) {
-                    stopped = true;
-                    break;
-                }
-                const uint32_t nb = uint32_t(p) - b * R < R ? uint32_t(p) - b * R : R;
-                const uint32_t slot = smem_addr(in_base + size_t(s) * R * TB);
-                uint32_t k0 = 0;
-                if (b == 0) {
-                    bulk_store(dst, slot, bytes);      // the first contribution lands first
-                    bulk_commit();
-                    bulk_wait_all();
-                    k0 = 1;
-                }
-                for (uint32_t k = k0; k < nb; ++k) BulkRed<T, OP>::issue(dst, slot + k * TB, bytes);
+            const uint32_t nb = uint32_t(p) - b * R < R ? uint32_t(p) - b * R : R;
+            const uint32_t slot = smem_addr(in_base + size_t(s) * R * TB);
+            uint32_t k0 = 0;
+            if (b == 0) {
+                bulk_store(dst, slot, bytes);      // the first contribution lands first
                 bulk_commit();
-                bulk_wait_read(0);                     // slots read: the stage may be refilled
-                mbar_arrive(smem_addr(&empty[s]));
-                ctl->consumed = i + 1;
+                bulk_wait_all();
+                k0 = 1;
             }
+            for (uint32_t k = k0; k < nb; ++k) BulkRed<T, OP>::issue(dst, slot + k * TB, bytes);
+            bulk_commit();
+            bulk_wait_read(0);                     // slots read: the stage may be refilled
+            mbar_arrive(smem_addr(&empty[s]));
+            ctl->consumed = i + 1;
         }
         bulk_wait_all();
     }
@@ -176,6 +184,12 @@ __global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
             const uint64_t t0 = global_ns();
             while (!mbar_try_wait(bar, (q / S) & 1u))
                 if (global_ns() - t0 > uint64_t(a.wait_ns)) break;
+        }
+    }
+    if (a.dynamic && threadIdx.x == 0) {
+        if (atomicAdd(a.status + 6, 1u) == gridDim.x - 1) {
+            atomicExch(reinterpret_cast<unsigned long long *>(a.status + 4), 0ull);
+            atomicExch(a.status + 6, 0u);
         }
     }
 }
@@ -209,7 +223,6 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
     a.status = L.status;
     a.wait_ns = L.wait_limit_ns;
     a.stall_test = 0;
-    a.dynamic = 0;
     a.ranks_per_stage = ranks;
 
     auto kern = bulkred_kernel<T, OP, P>;
@@ -240,6 +253,9 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
     }
     const uint64_t ctas = (tiles + pipes - 1) / pipes;
     const int grid = int(ctas < cap ? (ctas ? ctas : 1) : cap);
+    // the tile counter (as in the TMA variant): p=8 5236 -> 5565 GB/s, p=16
+    // 5023 -> 5501, p=64 5118 -> 5570 on every SM; 4 % slower at p=2
+    a.dynamic = L.tile_counter && tiles >= 16ull * uint64_t(grid) * pipes ? 1 : 0;
     const int block = int(pipes) * kBulkThreads;
     cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(block), smem, L.stream, a);
     if (err != cudaSuccess) return err;
