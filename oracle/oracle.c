@@ -22,8 +22,8 @@
  *  - "MSCCL, in depth", section "Writing an algorithm in MSCCLang": the
  *    all-pairs schedule scatters slice r of every rank to its owner r, which
  *    reduces it, then gathers.  The accumulation order used here for slice r
- *    is rank 0, 1, ..., p-1 (the plainest reading of "reduced at owner r in
- *    rank order").
+ *    is rank 0, 1, ..., p-1: the owner folds the contributions in rank order
+ *    (a reading; the page fixes no order inside the owner's reduction).
  *  - T-CCL, section "Shard Ownership": P shards, one per rank, the owner
  *    produces the final value of its shard (ReduceScatter), which then goes
  *    to every rank (AllGather).
@@ -37,7 +37,9 @@
  *  - min/max: acc = (v < acc) ? v : acc (resp. >): the earlier operand wins
  *    ties, so the schedule order fixes which of +0/-0 survives.
  *  - int32: sum and prod wrap modulo 2^32; avg is the wrapped sum divided by
- *    p with C division (truncation toward zero).
+ *    p with C division (truncation toward zero).  Parity unpinned for the
+ *    rounding of that division when the sum is not a multiple of p: the
+ *    pages fix no rounding, and the pins cover divisible sums only.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared -o liboracle.so oracle.c -lm
  */
