@@ -46,6 +46,8 @@ struct ReduceArgs {
     int p;
     int vec;                    // 1: 16-byte groups allowed (all pointers aligned)
     float scale;                // avg: fl32(1/p)
+    unsigned *status;           // status block: words 8-9 group counter, 10 finished CTAs
+    int dynamic;                // 1: warps beyond their first block take groups from the counter
 };
 
 // One element e of chunk c, folded in the chunk's order.
@@ -67,7 +69,7 @@ __device__ __forceinline__ void reduce_one(const ReduceArgs<PM> &a, int p, int c
 
 // P > 0: p fixed at compile time (loads fully unrolled); P == 0: any p up to
 // kMaxRanks, loads issued eight at a time.
-template <typename T, int OP, int P, int MODE>
+template <typename T, int OP, int P, int MODE, bool DYN>
 __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRanks)> &a)
 {
     using Tr = Traits<T>;
@@ -90,7 +92,7 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
         for (int k = 0; k < P; ++k) sp[k] = static_cast<const char *>(a.src[a.order[0][k]]);
     }
 
-    for (uint64_t g = tid; g < ngroups; g += stride) {
+    auto group = [&](uint64_t g) {
         const uint64_t e = g * VEC;
         if (e >= cend) {  // next chunk(s); empty chunks are skipped
             do { ++c; } while (e >= a.bound[c + 1]);
@@ -106,7 +108,7 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
                 while (e + j >= a.bound[cj + 1]) ++cj;
                 reduce_one<T, OP, MODE>(a, p, cj, e + j);
             }
-            continue;
+            return;
         }
         Acc acc[VEC];
         if constexpr (P > 0) {
@@ -159,6 +161,32 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
         } else {
             st_stream_v4(static_cast<char *>(a.dst[c]) + (e - a.bound[c]) * S, out);
         }
+    };
+    if (!DYN || !a.dynamic) {
+        for (uint64_t g = tid; g < ngroups; g += stride) group(g);
+    } else {
+        // Each warp takes blocks of 32 * kWarpGrab consecutive groups: its
+        // first statically, the rest from the status block's group counter,
+        // so that SMs that run faster take more -- with no CTA barrier (a
+        // CTA-wide grab cost more in barriers than it gained).  Measured at
+        // p=16 on 90 SMs: 6545 -> 6866 GB/s; p=2 on 76 SMs 5046 -> 5272; no
+        // change at 8-32 SMs.
+        constexpr int kWarpGrab = 16;
+        const uint32_t lane = threadIdx.x & 31u;
+        const uint64_t per = 32ull * kWarpGrab;
+        const uint64_t warps = uint64_t(gridDim.x) * (blockDim.x / 32);
+        unsigned long long *next = reinterpret_cast<unsigned long long *>(a.status + 8);
+        uint64_t base = (uint64_t(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * per;
+        while (base < ngroups) {
+            unsigned long long nb = 0;
+            if (lane == 0) nb = warps * per + atomicAdd(next, (unsigned long long)per);
+#pragma unroll 1
+            for (int j = 0; j < kWarpGrab; ++j) {
+                const uint64_t g = base + lane + uint64_t(j) * 32;
+                if (g < ngroups) group(g);
+            }
+            base = __shfl_sync(0xffffffffu, nb, 0);
+        }
     }
 
     // Elements after the last whole group (every element when vec == 0).
@@ -179,7 +207,7 @@ __global__ void __launch_bounds__(reduce_threads<P>())
 {
     grid_dependency_wait();
     grid_dependents_launch();
-    reduce_body<T, OP, P, MODE>(a);
+    reduce_body<T, OP, P, MODE, false>(a);
 }
 
 // SM budget: one large CTA per SM, so the full register file per thread.
@@ -189,7 +217,14 @@ __global__ void __launch_bounds__(reduce_budget_threads<P>(), 1)
     reduce_budget_kernel(const __grid_constant__ ReduceArgs<(P > 0 ? P : kMaxRanks)> a)
 {
     grid_dependency_wait();
-    reduce_body<T, OP, P, MODE>(a);
+    reduce_body<T, OP, P, MODE, true>(a);
+    if (a.dynamic) {
+        __syncthreads();
+        if (threadIdx.x == 0 && atomicAdd(a.status + 10, 1u) == gridDim.x - 1) {
+            atomicExch(reinterpret_cast<unsigned long long *>(a.status + 8), 0ull);
+            atomicExch(a.status + 10, 0u);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -212,6 +247,8 @@ static cudaError_t launch_p(const Launch &L, LaunchInfo *info)
     a.p = L.p;
     a.vec = L.vec ? 1 : 0;
     a.scale = 1.0f / float(L.p);
+    a.status = L.status;
+    a.dynamic = 0;
 
     // An SM budget takes the persistent large-CTA kernel, unless the whole
     // message already fits in at most `budget` small CTAs (small messages:
@@ -238,6 +275,11 @@ static cudaError_t launch_p(const Launch &L, LaunchInfo *info)
         }
     }
     const int grid = int(want < cap ? want : cap);
+    if (budget && a.vec) {
+        // the counter pays off once every warp has about 16 blocks to take
+        const uint64_t ngroups = L.n / Traits<T>::VEC;
+        a.dynamic = ngroups >= 16ull * 32 * 16 * uint64_t(kThreads / 32) * uint64_t(grid) ? 1 : 0;
+    }
     cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(kThreads), smem, L.stream, a);
     if (err != cudaSuccess) return err;
     if (info) {
