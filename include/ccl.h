@@ -66,9 +66,10 @@
  *
  * Threads and streams.  A communicator must not be used from two host
  * threads at once.  Its collectives must also be ordered on the device: issue
- * them on one stream, or order the streams.  The TMA variants hand out tiles
- * from a counter in the communicator's status block, so two collectives of
- * one communicator running at the same time would share it.  Different
+ * them on one stream, or order the streams.  On large messages the TMA
+ * variants and the SM-budget ld/st kernel hand out work from counters in the
+ * communicator's status block, so two collectives of one communicator
+ * running at the same time would share them.  Different
  * communicators are independent.  ccl_last_error() is per host thread.
  */
 #ifndef CCL_H
