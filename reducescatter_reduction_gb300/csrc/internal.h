@@ -69,8 +69,10 @@ constexpr size_t kTmaCtlBytes = 128;
 
 inline bool tma_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stages, size_t *smem)
 {
-    // 16 KB at p <= 3 (p=2: 7112 vs 6712 GB/s with 8 KB; p=3: 7070 vs 6413)
-    size_t T = want_tile ? want_tile : (p <= 3 ? 16384 : p <= 8 ? 8192 : p <= 16 ? 4096 : p <= 32 ? 2048 : 1024);
+    // measured on GB300 (bf16, all SMs): 16 KB at p <= 3 (p=2: 7112 vs 6712
+    // GB/s with 8 KB; p=3: 7070 vs 6413); 4 KB up to p = 24, where two stages
+    // of 4 KB still fit (p=20: 7000 vs 6234 with 2 KB; p=24: 6993 vs 6622)
+    size_t T = want_tile ? want_tile : (p <= 3 ? 16384 : p <= 8 ? 8192 : p <= 24 ? 4096 : p <= 32 ? 2048 : 1024);
     for (; T >= 1024; T /= 2) {
         const size_t per_stage = size_t(p + 1) * T;
         size_t S = (kTmaSmemLimit - 2 * kTmaMaxStages * 8 - kTmaCtlBytes) / per_stage;
