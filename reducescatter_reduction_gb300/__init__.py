@@ -128,7 +128,14 @@ def _params(params):
 # entry points
 # --------------------------------------------------------------------------
 
+def _want_len(ptrs, p: int, what: str):
+    # the C side reads exactly p pointers: a shorter list would be read past its end
+    if ptrs is not None and len(ptrs) != int(p):
+        raise CclError(CCL_ERR_INVALID_ARG, f"{what} has {len(ptrs)} pointers, p = {int(p)}")
+
+
 def ccl_comm_create(p: int, rank_ptrs) -> int:
+    _want_len(rank_ptrs, p, "rank_ptrs")
     h = ctypes.c_void_p()
     _check(load_library().ccl_comm_create(ctypes.byref(h), int(p), _ptr_array(rank_ptrs)))
     return h.value
@@ -181,6 +188,8 @@ def ccl_allreduce_static(p: int, in_ptrs, out_ptrs, op, dtype, n: int, schedule=
                          stream: int = 0) -> None:
     """The allocation-free AllReduce (see include/ccl.h): for callers that may
     not allocate device memory; needs no communicator."""
+    _want_len(in_ptrs, p, "in_ptrs")
+    _want_len(out_ptrs, p, "out_ptrs")
     _check(load_library().ccl_allreduce_static(int(p), _ptr_array(in_ptrs), _ptr_array(out_ptrs),
                                                _code(OPS, op), _code(DTYPES, dtype), int(n),
                                                _code(SCHEDULES, schedule), stream or None))

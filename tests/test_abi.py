@@ -170,3 +170,13 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(ccl, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         ccl.load_library(str(tmp_path / "libccl.so"))
+
+
+def test_binding_refuses_pointer_lists_of_the_wrong_length():
+    # the C side reads exactly p pointers; the binding checks the list first
+    with pytest.raises(ccl.CclError) as ei:
+        ccl.ccl_comm_create(3, [16, 32])
+    assert ei.value.status == ccl.CCL_ERR_INVALID_ARG and "p = 3" in str(ei.value)
+    with pytest.raises(ccl.CclError) as ei:
+        ccl.ccl_allreduce_static(2, [16, 32], [16], "sum", "f32", 8)
+    assert ei.value.status == ccl.CCL_ERR_INVALID_ARG

@@ -107,7 +107,7 @@ def test_static_entry_rejects_what_it_cannot_take():
         ccl.ccl_allreduce_static(p, ins.ptrs(), [outs.ptr(0)] * p, "sum", "bf16", n - 4, "ring", stream_ptr())
     assert ei.value.status == ccl.CCL_ERR_INVALID_ARG
     with pytest.raises(ccl.CclError) as ei:
-        ccl.ccl_allreduce_static(65, ins.ptrs() * 17, outs.ptrs() * 17, "sum", "bf16", 0, "ring", stream_ptr())
+        ccl.ccl_allreduce_static(65, (ins.ptrs() * 17)[:65], (outs.ptrs() * 17)[:65], "sum", "bf16", 0, "ring", stream_ptr())
     assert ei.value.status == ccl.CCL_ERR_INVALID_ARG
     with pytest.raises(ccl.CclError) as ei:
         ccl.ccl_allreduce_static(p, ins.ptrs(), outs.ptrs(), "sum", "bf16", n - 4, "custom", stream_ptr())
