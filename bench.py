@@ -343,6 +343,8 @@ def run_ours(args, dist: Dist):
         del outs
         torch.cuda.empty_cache()
         result["sweep"] = run_sweep(dist, dev, sptr, stream, peak, l2, ins)
+    if not args.no_sweep:
+        result["op_coverage"] = run_ops(dev, sptr, stream, peak)
     if not args.no_budgets:
         torch.cuda.empty_cache()
         result["sm_budgets"] = run_budgets(dev, sptr, stream, peak)
@@ -484,6 +486,53 @@ def run_variants(comm, sptr, stream, peak, n, args):
                          "launch": ccl.ccl_comm_last_launch(comm)}
     ccl.ccl_set_launch(comm, args.sm_budget, args.variant, 0)
     ccl.ccl_comm_check(comm)
+    return rows
+
+
+def run_ops(dev, sptr, stream, peak):
+    """The op-coverage workload: p=8 rank buffers of 64 Mi elements, ring,
+    every op in int32 (uniform in [-1000, 1000]; prod over {-1, 1, 2}), fp32
+    and fp16 (N(0,1)), drawn on the device.  GB/s over 2*p*n*s per call."""
+    import torch
+    import reducescatter_reduction_gb300 as ccl
+    from reducescatter_reduction_gb300 import inputs
+
+    p, n = 8, inputs.COVERAGE_N
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    rows = {}
+    for dtype, tdt, s in (("i32", torch.int32, 4), ("f32", torch.float32, 4), ("f16", torch.float16, 2)):
+        for op in ("sum", "prod", "min", "max", "avg"):
+            if dtype == "i32":
+                if op == "prod":
+                    vals = torch.tensor([-1, 1, 2], device=dev, dtype=torch.int32)
+                    ins = [vals[torch.randint(0, 3, (n,), generator=gen, device=dev)] for _ in range(p)]
+                else:
+                    ins = [torch.randint(-1000, 1001, (n,), generator=gen, device=dev, dtype=torch.int32)
+                           for _ in range(p)]
+            else:
+                ins = [torch.randn(n, generator=gen, device=dev).to(tdt) for _ in range(p)]
+            outs = [torch.empty_like(t) for t in ins]
+            h = ccl.ccl_comm_create(p, [t.data_ptr() for t in ins])
+            ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
+            for _ in range(3):
+                ccl.ccl_allreduce(h, op, dtype, n, "ring", sptr)
+            torch.cuda.synchronize()
+            iters = 20
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(iters):
+                ccl.ccl_allreduce(h, op, dtype, n, "ring", sptr)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ccl.ccl_comm_check(h)
+            us = e0.elapsed_time(e1) * 1e3 / iters
+            gbs = 2 * p * n * s / (us * 1e-6) / 1e9
+            rows[f"{dtype}_{op}"] = {"us": round(us, 1), "GBps": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4)}
+            ccl.ccl_comm_destroy(h)
+            del ins, outs
+    torch.cuda.empty_cache()
     return rows
 
 

@@ -41,9 +41,11 @@
  * 2^32.  The ld/st and TMA copy variants and the one-phase executor keep this
  * order exactly (identical bits); the TMA bulk-reduce variant
  * (CCL_VARIANT_TMA_BULKRED) lets the memory system apply the adds and is held
- * to |err| <= 2 * p * eps(element type) * sum_k |x_k| per element instead; the
- * stepwise-ring executor rounds each partial to the element type at every hop
- * (see ccl_variant_t).
+ * to |err| <= 2 * p * eps(element type) * sum_k |x_k| per element instead (its
+ * min/max pick the same value, but which of +0 and -0, or which NaN, is not
+ * fixed); the stepwise-ring executor rounds each partial to the element type
+ * at every hop (see ccl_variant_t).  A NaN that min/max keep is the input's
+ * own bit pattern for fp16/bf16.
  *
  * Memory and ownership.  The caller allocates and owns every rank buffer
  * (device memory, e.g. from PyTorch).  A communicator copies the p input and

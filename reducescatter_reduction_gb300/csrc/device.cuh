@@ -267,4 +267,101 @@ template <int OP> struct FoldI {
 template <typename T, int OP>
 using Fold = typename std::conditional<std::is_same<T, I32>::value, FoldI<OP>, FoldF<OP>>::type;
 
+// ---------------------------------------------------------------------------
+// The fold of one 16-byte group per rank: `first` takes the first rank's
+// group, `fold` each later one in order, `finish` returns the packed result.
+// In general the lanes are widened to fp32 (or uint32) and folded with Fold.
+// ---------------------------------------------------------------------------
+
+template <typename T, int OP, typename Enable = void>
+struct GroupFold {
+    using Tr = Traits<T>;
+    using F = Fold<T, OP>;
+    typename Tr::Acc acc[Tr::VEC];
+
+    __device__ __forceinline__ void first(const uint4 &r, float scale)
+    {
+        typename Tr::Acc v[Tr::VEC];
+        Tr::unpack(r, v);
+#pragma unroll
+        for (int i = 0; i < Tr::VEC; ++i) acc[i] = F::first(v[i], scale);
+    }
+    __device__ __forceinline__ void fold(const uint4 &r, float scale)
+    {
+        typename Tr::Acc v[Tr::VEC];
+        Tr::unpack(r, v);
+#pragma unroll
+        for (int i = 0; i < Tr::VEC; ++i) acc[i] = F::fold(acc[i], v[i], scale);
+    }
+    __device__ __forceinline__ uint4 finish(int p)
+    {
+#pragma unroll
+        for (int i = 0; i < Tr::VEC; ++i) acc[i] = F::finish(acc[i], p);
+        return Tr::pack(acc);
+    }
+};
+
+// min/max of fp16 or bf16: the result is one of the inputs, so no lane needs
+// widening or rounding.  Pairs of lanes are compared in place with the
+// ordered IEEE comparison (false for NaN; -0 equals +0) and the later rank's
+// lane replaces the accumulator's only where it compares strictly less
+// (min) or greater (max) -- the operand the fp32 compare-and-select keeps,
+// bit for bit, since the widening is exact and preserves order.  Measured on
+// GB300 (ld/st AllReduce, fp16 and bf16 alike): p=8 over 64 Mi elements
+// 6.04 -> 6.67 TB/s, p=16 over 112 Mi 5.89 -> 6.72 TB/s.  The rest of the
+// gap to sum (7.04) is the compare -> select dependency chain, which keeps
+// each CTA resident longer with no loads in flight; issuing every load before
+// the first compare changed nothing.
+template <typename T> struct Pair16;
+template <> struct Pair16<F16> {
+    __device__ static __forceinline__ uint32_t lt(uint32_t a, uint32_t b)
+    {
+        return __hlt2_mask(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+    }
+    __device__ static __forceinline__ uint32_t gt(uint32_t a, uint32_t b)
+    {
+        return __hgt2_mask(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+    }
+};
+template <> struct Pair16<BF16> {
+    __device__ static __forceinline__ uint32_t lt(uint32_t a, uint32_t b)
+    {
+        return __hlt2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&a), *reinterpret_cast<const __nv_bfloat162 *>(&b));
+    }
+    __device__ static __forceinline__ uint32_t gt(uint32_t a, uint32_t b)
+    {
+        return __hgt2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&a), *reinterpret_cast<const __nv_bfloat162 *>(&b));
+    }
+};
+
+template <typename T, int OP>
+constexpr bool kSelect16 = (std::is_same<T, F16>::value || std::is_same<T, BF16>::value) &&
+                           (OP == OP_MIN || OP == OP_MAX);
+
+template <typename T, int OP>
+struct GroupFold<T, OP, typename std::enable_if<kSelect16<T, OP>>::type> {
+    uint32_t w[4];
+
+    __device__ static __forceinline__ uint32_t pick(uint32_t acc, uint32_t v)
+    {
+        const uint32_t m = OP == OP_MIN ? Pair16<T>::lt(v, acc) : Pair16<T>::gt(v, acc);
+        return (v & m) | (acc & ~m);
+    }
+    __device__ __forceinline__ void first(const uint4 &r, float)
+    {
+        w[0] = r.x;
+        w[1] = r.y;
+        w[2] = r.z;
+        w[3] = r.w;
+    }
+    __device__ __forceinline__ void fold(const uint4 &r, float)
+    {
+        w[0] = pick(w[0], r.x);
+        w[1] = pick(w[1], r.y);
+        w[2] = pick(w[2], r.z);
+        w[3] = pick(w[3], r.w);
+    }
+    __device__ __forceinline__ uint4 finish(int) { return make_uint4(w[0], w[1], w[2], w[3]); }
+};
+
 }  // namespace ccl

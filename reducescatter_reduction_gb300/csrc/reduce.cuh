@@ -56,6 +56,27 @@ __device__ __forceinline__ void reduce_one(const ReduceArgs<PM> &a, int p, int c
 {
     using Tr = Traits<T>;
     using F = Fold<T, OP>;
+    if constexpr (kSelect16<T, OP>) {
+        // min/max of a 16-bit type: keep the chosen input's own bits, as the
+        // packed group fold does (the fp32 compare picks the same operand)
+        const uint16_t *s0 = static_cast<const uint16_t *>(a.src[a.order[c][0]]);
+        uint16_t keep = s0[e];
+        float acc = Tr::load1(s0, e);
+        for (int k = 1; k < p; ++k) {
+            const uint16_t *sk = static_cast<const uint16_t *>(a.src[a.order[c][k]]);
+            const float v = Tr::load1(sk, e);
+            if (OP == OP_MIN ? v < acc : v > acc) {
+                acc = v;
+                keep = sk[e];
+            }
+        }
+        if constexpr (MODE == MODE_AR) {
+            for (int k = 0; k < p; ++k) static_cast<uint16_t *>(a.dst[k])[e] = keep;
+        } else {
+            static_cast<uint16_t *>(a.dst[c])[e - a.bound[c]] = keep;
+        }
+        return;
+    }
     auto acc = F::first(Tr::load1(a.src[a.order[c][0]], e), a.scale);
     for (int k = 1; k < p; ++k)
         acc = F::fold(acc, Tr::load1(a.src[a.order[c][k]], e), a.scale);
@@ -73,7 +94,6 @@ template <typename T, int OP, int P, int MODE, bool DYN>
 __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRanks)> &a)
 {
     using Tr = Traits<T>;
-    using F = Fold<T, OP>;
     using Acc = typename Tr::Acc;
     constexpr int VEC = Tr::VEC;
     constexpr int ES = int(sizeof(Acc));     // element bytes of the 4-byte types
@@ -110,21 +130,14 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
             }
             return;
         }
-        Acc acc[VEC];
+        GroupFold<T, OP> acc;
         if constexpr (P > 0) {
             uint4 r[P];
 #pragma unroll
             for (int k = 0; k < P; ++k) r[k] = ld_stream_v4(sp[k] + e * S);
-            Acc v[VEC];
-            Tr::unpack(r[0], v);
+            acc.first(r[0], a.scale);
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) acc[i] = F::first(v[i], a.scale);
-#pragma unroll
-            for (int k = 1; k < P; ++k) {
-                Tr::unpack(r[k], v);
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) acc[i] = F::fold(acc[i], v[i], a.scale);
-            }
+            for (int k = 1; k < P; ++k) acc.fold(r[k], a.scale);
         } else {
             for (int k0 = 0; k0 < p; k0 += 8) {
                 uint4 r[8];
@@ -135,22 +148,13 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     if (k0 + j < p) {
-                        Acc v[VEC];
-                        Tr::unpack(r[j], v);
-                        if (k0 + j == 0) {
-#pragma unroll
-                            for (int i = 0; i < VEC; ++i) acc[i] = F::first(v[i], a.scale);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < VEC; ++i) acc[i] = F::fold(acc[i], v[i], a.scale);
-                        }
+                        if (k0 + j == 0) acc.first(r[j], a.scale);
+                        else acc.fold(r[j], a.scale);
                     }
                 }
             }
         }
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) acc[i] = F::finish(acc[i], p);
-        const uint4 out = Tr::pack(acc);
+        const uint4 out = acc.finish(p);
         if constexpr (MODE == MODE_AR) {
             if constexpr (P > 0) {
 #pragma unroll

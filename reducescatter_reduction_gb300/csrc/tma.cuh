@@ -300,33 +300,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             const uint32_t in_s = smem_addr(in_base + size_t(s) * p * TB);
             const uint32_t out_s = smem_addr(out_base + size_t(s) * TB);
             for (uint32_t g = tid; g < bytes / 16; g += kTmaConsumers) {
-                Acc acc[VEC], v[VEC];
+                GroupFold<T, OP> acc;
                 if constexpr (P > 0) {
                     uint4 r[P];
 #pragma unroll
                     for (int k = 0; k < P; ++k) r[k] = lds_v4(in_s + k * TB + g * 16);
-                    Tr::unpack(r[0], v);
+                    acc.first(r[0], a.scale);
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) acc[e] = F::first(v[e], a.scale);
-#pragma unroll
-                    for (int k = 1; k < P; ++k) {
-                        Tr::unpack(r[k], v);
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) acc[e] = F::fold(acc[e], v[e], a.scale);
-                    }
+                    for (int k = 1; k < P; ++k) acc.fold(r[k], a.scale);
                 } else {
-                    Tr::unpack(lds_v4(in_s + g * 16), v);
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) acc[e] = F::first(v[e], a.scale);
-                    for (int k = 1; k < p; ++k) {
-                        Tr::unpack(lds_v4(in_s + k * TB + g * 16), v);
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) acc[e] = F::fold(acc[e], v[e], a.scale);
-                    }
+                    acc.first(lds_v4(in_s + g * 16), a.scale);
+                    for (int k = 1; k < p; ++k) acc.fold(lds_v4(in_s + k * TB + g * 16), a.scale);
                 }
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) acc[e] = F::finish(acc[e], p);
-                sts_v4(out_s + g * 16, Tr::pack(acc));
+                sts_v4(out_s + g * 16, acc.finish(p));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&empty[s]));  // input slots of stage s are free
@@ -468,7 +454,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     } else {
         // ------------------------------ consumers -----------------------------
         const int tid = threadIdx.x - 32;
-        Acc acc[kTmaWideGroups][VEC];
+        GroupFold<T, OP> acc[kTmaWideGroups];
         int c = 0;
         uint32_t k = 0;  // tiles finished (output tile k & 1)
         for (uint32_t i = 0;; ++i) {
@@ -490,16 +476,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             for (int q = 0; q < kTmaWideGroups; ++q) {
                 const uint32_t g = uint32_t(tid) + uint32_t(q) * kTmaConsumers;
                 if (g * 16 >= bytes) continue;
-                Acc v[VEC];
                 for (uint32_t j = 0; j < nb; ++j) {
-                    Tr::unpack(lds_v4(in_s + j * TB + g * 16), v);
-                    if (b == 0 && j == 0) {
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) acc[q][e] = F::first(v[e], a.scale);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) acc[q][e] = F::fold(acc[q][e], v[e], a.scale);
-                    }
+                    const uint4 r = lds_v4(in_s + j * TB + g * 16);
+                    if (b == 0 && j == 0) acc[q].first(r, a.scale);
+                    else acc[q].fold(r, a.scale);
                 }
             }
             __syncwarp();
@@ -515,9 +495,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 for (int q = 0; q < kTmaWideGroups; ++q) {
                     const uint32_t g = uint32_t(tid) + uint32_t(q) * kTmaConsumers;
                     if (g * 16 >= bytes) continue;
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) acc[q][e] = F::finish(acc[q][e], p);
-                    sts_v4(out_s + g * 16, Tr::pack(acc[q]));
+                    sts_v4(out_s + g * 16, acc[q].finish(p));
                 }
                 fence_proxy_async_smem();                      // out tile visible to the bulk stores
                 consumer_barrier();

@@ -88,6 +88,25 @@ def choice(n: int, seed: int, rank: int, values, dtype: str) -> np.ndarray:
     return store(v.astype(np.float32), dtype)
 
 
+# IEEE special values of the 16-bit float types, as bit patterns: +0 and -0,
+# the smallest and the largest subnormal, the smallest normal, 1 and the next
+# value above it, the largest finite value, infinity, and the quiet NaN of the
+# conversions' canonical form -- each with both signs.
+SPECIAL_BITS = {
+    "f16": [0x0000, 0x0001, 0x03FF, 0x0400, 0x3C00, 0x3C01, 0x7BFF, 0x7C00, 0x7E00],
+    "bf16": [0x0000, 0x0001, 0x007F, 0x0080, 0x3F80, 0x3F81, 0x7F7F, 0x7F80, 0x7FC0],
+}
+
+
+def specials(n: int, seed: int, rank: int, dtype: str, nan: bool = True) -> np.ndarray:
+    """Raw 16-bit patterns drawn uniformly from SPECIAL_BITS[dtype] and their
+    negatives (NaN left out when ``nan`` is false).  Few distinct values, so
+    ties (and +0 against -0) are frequent."""
+    vals = [b for b in SPECIAL_BITS[dtype] if nan or b not in (0x7E00, 0x7FC0)]
+    table = np.asarray(vals + [b | 0x8000 for b in vals], dtype=np.uint16)
+    return table[rng(seed, rank).integers(0, len(table), size=n)]
+
+
 def worked(p: int = 2, n: int = 4096):
     """Uniform ints in [-8, 8] as fp32; ranks 0 and 1 start with the worked example."""
     xs = [uniform_int(n, SEEDS["worked"], r, -8, 8, "f32") for r in range(p)]

@@ -679,3 +679,22 @@ def test_rmsnorm_closed_form_with_eps():
     gamma = to_storage([1.0, 1.0], "f32")
     out, _ = oracle.allreduce_residual_rmsnorm(xs, res, gamma, 1, 2, "f32", eps=0.5)
     assert np.array_equal(out, np.float32(np.array([3.0, 4.0]) / math.sqrt(13.0)))
+
+
+@pytest.mark.parametrize("dtype,one,nan,ninf,sub", [("f16", 0x3C00, 0x7E00, 0xFC00, 0x0001),
+                                                      ("bf16", 0x3F80, 0x7FC0, 0xFF80, 0x0001)])
+def test_min_max_special_values_follow_compare_and_select(dtype, one, nan, ninf, sub):
+    """min/max keep the earlier operand unless the later one compares
+    strictly less (greater): +0 against -0 keeps whichever came first, a NaN
+    stays only when it comes first, infinities and subnormals order as
+    numbers.  All-pairs order folds rank 0 then rank 1."""
+    pz, nz = 0x0000, 0x8000
+    x0 = np.array([pz, nz, nan, one, ninf, sub, nz | sub, pz], dtype=np.uint16)
+    x1 = np.array([nz, pz, one, nan, nz, pz, nz, nan | 0x8000], dtype=np.uint16)
+    mn = oracle.allreduce([x0, x1], "min", dtype, "allpairs")[0]
+    mx = oracle.allreduce([x0, x1], "max", dtype, "allpairs")[0]
+    assert mn.tolist() == [pz, nz, nan, one, ninf, pz, nz | sub, pz]
+    assert mx.tolist() == [pz, nz, nan, one, nz, sub, nz, pz]
+    # ring order for p = 2: chunk 0 folds rank 1 then rank 0
+    ring = oracle.allreduce([x0, x1], "min", dtype, "ring")[0]
+    assert ring[:4].tolist() == [nz, pz, one, nan]

@@ -660,3 +660,37 @@ def test_concurrent_communicators_on_separate_streams():
             assert bits_equal(outs.host(r), want[r]), (p, dtype, op, r)
         ccl.ccl_comm_check(h)
         ccl.ccl_comm_destroy(h)
+
+
+# ---------------------------------------------------------------------------
+# min/max on IEEE special values (fp16/bf16 fold packed pairs in place)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("op", ["min", "max"])
+@pytest.mark.parametrize("p,variant,budget", [(8, "ldst", 0), (3, "ldst", 0), (5, "ldst", 0), (8, "ldst", 4),
+                                              (16, "ldst", 0), (8, "tma", 0), (5, "tma", 0), (40, "tma", 0)])
+def test_min_max_special_values(dtype, op, p, variant, budget):
+    """Signed zeros, subnormals, infinities and quiet NaNs of both signs,
+    drawn so that ties are frequent: bit-identical to the oracle's
+    compare-and-select (earlier operand wins ties; a NaN only if it comes
+    first), AllReduce and ReduceScatter, both schedules."""
+    n = p * 8 * 1500
+    xs = [inputs.specials(n, 97, r, dtype) for r in range(p)]
+    for sched in ("ring", "allpairs"):
+        res, desc = run_collective(xs, "ar", op, dtype, sched, budget=budget, variant=variant)
+        want = oracle.allreduce(xs, op, dtype, sched)
+        for r in range(p):
+            assert bits_equal(res.host(r), want[r]), (sched, r, desc)
+        res, desc = run_collective(xs, "rs", op, dtype, sched, budget=budget, variant=variant)
+        want = oracle.reduce_scatter(xs, op, dtype, sched)
+        for r in range(p):
+            assert bits_equal(res.host(r), want[r]), (sched, r, desc)
+    if variant == "ldst":
+        # ragged: a group straddling a chunk boundary and a sub-group tail
+        m = n + 3
+        ys = [inputs.specials(m, 98, r, dtype) for r in range(p)]
+        res, desc = run_collective(ys, "ar", op, dtype, "ring", budget=budget, variant=variant)
+        want = oracle.allreduce(ys, op, dtype, "ring")
+        for r in range(p):
+            assert bits_equal(res.host(r), want[r]), (r, desc)
