@@ -343,6 +343,7 @@ def run_ours(args, dist: Dist):
         del outs
         torch.cuda.empty_cache()
         result["sweep"] = run_sweep(dist, dev, sptr, stream, peak, l2, ins)
+        result["launch_floor"] = launch_floor()
     if not args.no_sweep:
         result["op_coverage"] = run_ops(dev, sptr, stream, peak)
     if not args.no_budgets:
@@ -773,6 +774,37 @@ def graph_latency(comms, sets, n, sched, calls=200):
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) * 1e3 / (5 * calls)
+
+
+def launch_floor(calls=200):
+    """Per-launch time of an empty kernel (torch.cuda._sleep(0): one thread,
+    no memory access) replayed the same way as graph_latency: the floor the
+    small-message calls are measured against."""
+    import torch
+
+    if not hasattr(torch.cuda, "_sleep"):
+        return None
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(0)
+        side.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(calls):
+                torch.cuda._sleep(0)
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return {"us_graph": round(e0.elapsed_time(e1) * 1e3 / (5 * calls), 3),
+            "kernel": "empty kernel (torch.cuda._sleep(0)), ordinary launches, CUDA-graph replay"}
 
 
 def run_sweep(dist, dev, sptr, stream, peak, l2, big_inputs):
