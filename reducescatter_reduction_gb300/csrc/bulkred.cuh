@@ -226,11 +226,10 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
     a.ranks_per_stage = ranks;
 
     auto kern = bulkred_kernel<T, OP, P>;
-    static std::atomic<bool> attr{false};  // set once; racing first calls both set it
-    if (!attr.load(std::memory_order_acquire)) {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTmaSmemLimit));
+    static std::atomic<unsigned long long> attr{0};  // devices on which the limit is raised
+    {
+        const cudaError_t err = allow_dynamic_smem(kern, kTmaSmemLimit, L.device, attr);
         if (err != cudaSuccess) return err;
-        attr.store(true, std::memory_order_release);
     }
     const size_t pipe = bulkred_pipe_bytes(int(ranks), tile, stages);
     uint64_t cap;

@@ -482,6 +482,7 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     }
     L.vec = aligned && (coll == COLL_AR || (n / p * s) % 16 == 0);
     L.self_mask = self_mask;
+    L.device = c->device;
     L.num_sms = c->num_sms;
     L.sm_budget = c->sm_budget;
     L.pipe_bytes = c->pipe_bytes;
@@ -648,6 +649,7 @@ extern "C" ccl_status_t ccl_allreduce_residual_rmsnorm(ccl_comm_t c, ccl_dtype_t
         L.dst[r] = c->out[r];
         aligned = aligned && uintptr_t(c->in[r]) % 16 == 0 && uintptr_t(c->out[r]) % 16 == 0;
     }
+    L.device = c->device;
     L.num_sms = c->num_sms;
     L.stream = static_cast<cudaStream_t>(stream);
     const int sched = resolve_schedule(c, schedule, double(n) * double(s));

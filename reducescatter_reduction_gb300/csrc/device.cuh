@@ -91,6 +91,20 @@ static cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned grid, unsig
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// cudaFuncSetAttribute acts on the kernel as loaded for the current device,
+// so a raised dynamic shared-memory limit is set once per device: bit d of
+// `done` records device d (a device numbered 64 or more sets it every call).
+template <typename... KArgs>
+static cudaError_t allow_dynamic_smem(void (*kern)(KArgs...), size_t bytes, int device,
+                                      std::atomic<unsigned long long> &done)
+{
+    const unsigned long long bit = (device >= 0 && device < 64) ? (1ull << device) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    if (err == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return err;
+}
+
 // ---------------------------------------------------------------------------
 // Element types.  Each traits class gives: the accumulator type, VEC =
 // elements per 16 bytes, unpacking a 16-byte vector into VEC accumulator

@@ -99,11 +99,10 @@ static cudaError_t gather_launch(const Launch &L, LaunchInfo *info)
     if (budget) {
         cap = uint64_t(L.sm_budget);
         smem = 120 * 1024;  // at most one CTA per SM
-        static std::atomic<bool> attr{false};  // set once; racing first calls both set it
-        if (!attr.load(std::memory_order_acquire)) {
-            cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        static std::atomic<unsigned long long> attr{0};  // devices on which the limit is raised
+        {
+            const cudaError_t err = allow_dynamic_smem(kern, smem, L.device, attr);
             if (err != cudaSuccess) return err;
-            attr.store(true, std::memory_order_release);
         }
     }
     const int grid = int(want < cap ? want : cap);

@@ -39,6 +39,7 @@ struct Launch {
     const Table *table = nullptr;
     bool vec = false;          // 16-byte vector body allowed
     uint64_t self_mask = 0;    // AllGather: bit r set when dst[r] == src[r] (in place)
+    int device = 0;            // the current device while the kernel is launched
     int num_sms = 0;
     int sm_budget = 0;         // 0 = all SMs
     size_t pipe_bytes = 0;     // TMA stage bytes per rank

@@ -288,11 +288,10 @@ static cudaError_t launch_p(const Launch &L, LaunchInfo *info)
         // SM's shared memory so that no two fit on one SM
         cap = uint64_t(L.sm_budget);
         smem = 120 * 1024;
-        static std::atomic<bool> attr{false};  // set once; racing first calls both set it
-        if (!attr.load(std::memory_order_acquire)) {
-            cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        static std::atomic<unsigned long long> attr{0};  // devices on which the limit is raised
+        {
+            const cudaError_t err = allow_dynamic_smem(kern, smem, L.device, attr);
             if (err != cudaSuccess) return err;
-            attr.store(true, std::memory_order_release);
         }
     }
     const int grid = int(want < cap ? want : cap);

@@ -172,6 +172,7 @@ extern "C" ccl_status_t ccl_allreduce_static(int p, void *const *in_ptrs, void *
     }
     L.table = &table;
     L.vec = true;
+    L.device = dev;
     L.num_sms = num_sms;
     L.sm_budget = 0;
     L.pipe_bytes = 0;

@@ -571,11 +571,10 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
     a.stall_test = L.stall_test;
 
     auto kern = tma_reduce_kernel<T, OP, P, MODE>;
-    static std::atomic<bool> attr{false};  // set once; racing first calls both set it
-    if (!attr.load(std::memory_order_acquire)) {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTmaSmemLimit));
+    static std::atomic<unsigned long long> attr{0};  // devices on which the limit is raised
+    {
+        const cudaError_t err = allow_dynamic_smem(kern, kTmaSmemLimit, L.device, attr);
         if (err != cudaSuccess) return err;
-        attr.store(true, std::memory_order_release);
     }
     uint64_t cap = uint64_t(L.num_sms);
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) cap = uint64_t(L.sm_budget);
@@ -624,11 +623,10 @@ static cudaError_t tma_wide_launch(const Launch &L, LaunchInfo *info)
     a.stall_test = L.stall_test;
 
     auto kern = tma_wide_kernel<T, OP, MODE>;
-    static std::atomic<bool> attr{false};  // set once; racing first calls both set it
-    if (!attr.load(std::memory_order_acquire)) {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTmaSmemLimit));
+    static std::atomic<unsigned long long> attr{0};  // devices on which the limit is raised
+    {
+        const cudaError_t err = allow_dynamic_smem(kern, kTmaSmemLimit, L.device, attr);
         if (err != cudaSuccess) return err;
-        attr.store(true, std::memory_order_release);
     }
     uint64_t cap = uint64_t(L.num_sms);
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) cap = uint64_t(L.sm_budget);
