@@ -98,7 +98,7 @@ typedef struct ccl_comm *ccl_comm_t;
 typedef enum {
     CCL_OK = 0,
     CCL_ERR_INVALID_ARG = 1, /* bad pointer, size, alias, enum value, schedule table */
-    CCL_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (e.g. bulk-reduce of prod) */
+    CCL_ERR_UNSUPPORTED = 2, /* valid request the library does not serve (e.g. bulk-reduce of prod) */
     CCL_ERR_CUDA = 3,        /* a CUDA runtime call failed; ccl_last_error() names it */
     CCL_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (see ccl_comm_check) */
     CCL_ERR_NOMEM = 5        /* host or device allocation failed */

@@ -449,7 +449,7 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     if (variant == CCL_VARIANT_RING_STEPWISE && schedule != CCL_SCHED_AUTO && schedule != CCL_SCHED_RING)
         return fail(CCL_ERR_UNSUPPORTED, "the stepwise ring runs the ring schedule only");
     if ((variant == CCL_VARIANT_TMA || variant == CCL_VARIANT_TMA_BULKRED) && coll == COLL_AG)
-        return fail(CCL_ERR_UNSUPPORTED, "AllGather has no TMA variant in this build (use ld/st)");
+        return fail(CCL_ERR_UNSUPPORTED, "AllGather has no TMA variant (use ld/st)");
     if (variant == CCL_VARIANT_TMA_BULKRED && !bulkred_supported(dtype, op))
         return fail(CCL_ERR_UNSUPPORTED,
                     "the bulk-reduce variant has sum (f32/f16/bf16/i32) and min/max (f16/bf16/i32) only");
