@@ -51,7 +51,11 @@
  * (device memory, e.g. from PyTorch).  A communicator copies the p input and
  * output pointers (host arrays are not retained) and allocates one small
  * device status block (256 bytes) that it frees in ccl_comm_destroy().  No
- * call allocates memory proportional to the message.
+ * call allocates memory proportional to the message.  Rank buffers may also
+ * be page-locked host memory the device can address with the same pointer
+ * (cudaHostAlloc, or torch's pin_memory): the ld/st kernels then read and
+ * write it directly over the host link, with no staging copy (tested for
+ * AllReduce, ReduceScatter and AllGather with the ld/st variant).
  *
  * Asynchrony.  The collective calls check their arguments on the host,
  * enqueue kernels on `stream` (a cudaStream_t passed as void*, NULL = the

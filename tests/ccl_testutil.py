@@ -33,7 +33,9 @@ def to_numpy(t: torch.Tensor, storage) -> np.ndarray:
 class RankBuffers:
     """p device buffers of n elements, each inside its own allocation with a
     canary-filled guard band on both sides (offset shifts the data start by
-    that many bytes, for misaligned-pointer tests)."""
+    that many bytes, for misaligned-pointer tests).  device="pinned" puts
+    them in page-locked host memory instead, which the kernels address
+    directly."""
 
     def __init__(self, host: list[np.ndarray] | None, n: int, storage, p: int | None = None,
                  offset: int = 0, device="cuda"):
@@ -45,11 +47,15 @@ class RankBuffers:
         nbytes = n * self.s
         self.raw = []
         self.views = []
+        pinned = device == "pinned"
+        where = "cpu" if pinned else device
         for r in range(self.p):
-            raw = torch.full((GUARD + offset + nbytes + GUARD,), CANARY, dtype=torch.uint8, device=device)
+            raw = torch.full((GUARD + offset + nbytes + GUARD,), CANARY, dtype=torch.uint8, device=where)
+            if pinned:
+                raw = raw.pin_memory()
             body = raw[GUARD + offset: GUARD + offset + nbytes]
             if host is not None:
-                body.copy_(torch.from_numpy(host[r].view(np.uint8).reshape(-1)).to(device))
+                body.copy_(torch.from_numpy(host[r].view(np.uint8).reshape(-1)).to(where))
             self.raw.append(raw)
             self.views.append(body)
 

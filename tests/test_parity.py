@@ -41,13 +41,13 @@ def gen(dtype, op, p, n, seed):
 
 
 def run_collective(xs, coll, op, dtype, sched="ring", inplace=False, offset=0, budget=0,
-                   variant="ldst", n=None):
+                   variant="ldst", n=None, in_device="cuda", out_device="cuda"):
     storage = inputs.STORAGE[dtype]
     p = len(xs)
     n = xs[0].size if n is None else n
-    ins = RankBuffers(xs, n, storage, offset=offset)
+    ins = RankBuffers(xs, n, storage, offset=offset, device=in_device)
     out_n = n // p if coll == "rs" else n
-    outs = None if inplace else RankBuffers(None, out_n, storage, p=p, offset=offset)
+    outs = None if inplace else RankBuffers(None, out_n, storage, p=p, offset=offset, device=out_device)
     with Comm(ins, outs) as cm:
         ccl.ccl_set_launch(cm.h, budget, variant, 0)
         before = ccl.ccl_comm_launch_count(cm.h)
@@ -694,3 +694,33 @@ def test_min_max_special_values(dtype, op, p, variant, budget):
         want = oracle.allreduce(ys, op, dtype, "ring")
         for r in range(p):
             assert bits_equal(res.host(r), want[r]), (r, desc)
+
+
+# ---------------------------------------------------------------------------
+# page-locked host buffers, addressed by the kernels directly (zero-copy)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("coll", ["ar", "rs", "ag"])
+@pytest.mark.parametrize("where", [("pinned", "pinned"), ("pinned", "cuda"), ("cuda", "pinned")])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_host_buffers_zero_copy(coll, where, dtype):
+    """Rank buffers in page-locked host memory: the ld/st kernels read and
+    write them over the host link; bits equal the oracle's, and nothing is
+    written outside the buffers."""
+    p = 8
+    n = p * 40000 + (3 if coll == "ar" else 0)
+    op = "sum"
+    xs = gen(dtype, op, p, n, seed=61)
+    for inplace in (False, True):
+        if inplace and (where[0] != where[1] or coll == "rs"):
+            continue
+        res, desc = run_collective(xs, coll, op, dtype, "ring", inplace=inplace,
+                                   in_device=where[0], out_device=where[1])
+        if coll == "ag":
+            want = oracle.all_gather(xs, dtype)
+        elif coll == "rs":
+            want = oracle.reduce_scatter(xs, op, dtype, "ring")
+        else:
+            want = oracle.allreduce(xs, op, dtype, "ring")
+        for r in range(p):
+            assert bits_equal(res.host(r), want[r]), (coll, where, inplace, r, desc)
