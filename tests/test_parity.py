@@ -711,10 +711,10 @@ def test_host_buffers_zero_copy(coll, where, dtype):
     n = p * 40000 + (3 if coll == "ar" else 0)
     op = "sum"
     xs = gen(dtype, op, p, n, seed=61)
-    for inplace in (False, True):
+    for inplace, budget in ((False, 0), (True, 0), (False, 8)):
         if inplace and (where[0] != where[1] or coll == "rs"):
             continue
-        res, desc = run_collective(xs, coll, op, dtype, "ring", inplace=inplace,
+        res, desc = run_collective(xs, coll, op, dtype, "ring", inplace=inplace, budget=budget,
                                    in_device=where[0], out_device=where[1])
         if coll == "ag":
             want = oracle.all_gather(xs, dtype)
@@ -723,4 +723,4 @@ def test_host_buffers_zero_copy(coll, where, dtype):
         else:
             want = oracle.allreduce(xs, op, dtype, "ring")
         for r in range(p):
-            assert bits_equal(res.host(r), want[r]), (coll, where, inplace, r, desc)
+            assert bits_equal(res.host(r), want[r]), (coll, where, inplace, budget, r, desc)
