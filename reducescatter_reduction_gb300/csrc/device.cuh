@@ -325,7 +325,8 @@ struct GroupFold {
 // 6.04 -> 6.67 TB/s, p=16 over 112 Mi 5.89 -> 6.72 TB/s.  The rest of the
 // gap to sum (7.04) is the compare -> select dependency chain, which keeps
 // each CTA resident longer with no loads in flight; issuing every load before
-// the first compare changed nothing.
+// the first compare changed nothing, more CTAs per SM recover part of it at
+// p = 8 (reduce_kernel_occ5).
 template <typename T> struct Pair16;
 template <> struct Pair16<F16> {
     __device__ static __forceinline__ uint32_t lt(uint32_t a, uint32_t b)

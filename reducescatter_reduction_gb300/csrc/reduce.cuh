@@ -214,11 +214,6 @@ __global__ void __launch_bounds__(reduce_threads<P>())
     reduce_body<T, OP, P, MODE, false>(a);
 }
 
-// fp16/bf16 min/max at p = 8 (the packed select fold): the same body, with
-// five CTAs per SM asked of the compiler (48 registers, no spills) instead
-// of its own four.  The compare -> select chain keeps each thread's loads
-// outstanding for longer than a sum's adds do, so more resident threads pay:
-// 6.72 -> 6.89 TB/s on GB300 (six CTAs: 6.81; at p = 4 neither helped).
 // fp32 sum, prod and avg at p = 5 or 6 through the generic kernel: the same
 // body with eight 128-thread CTAs per SM asked of the compiler (64
 // registers, no spills) instead of its seven.  Measured on GB300 over 4 GiB
@@ -233,6 +228,11 @@ __global__ void __launch_bounds__(reduce_threads<P>(), 8)
     reduce_body<T, OP, P, MODE, false>(a);
 }
 
+// fp16/bf16 min/max at p = 8 (the packed select fold): the same body, with
+// five CTAs per SM asked of the compiler (48 registers, no spills) instead
+// of its own four.  The compare -> select chain keeps each thread's loads
+// outstanding for longer than a sum's adds do, so more resident threads pay:
+// 6.72 -> 6.89 TB/s on GB300 (six CTAs: 6.81; at p = 4 neither helped).
 template <typename T, int OP, int P, int MODE>
 __global__ void __launch_bounds__(reduce_threads<P>(), 5)
     reduce_kernel_occ5(const __grid_constant__ ReduceArgs<(P > 0 ? P : kMaxRanks)> a)

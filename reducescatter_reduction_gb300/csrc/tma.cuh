@@ -201,8 +201,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     tma_reduce_kernel(const __grid_constant__ TmaArgs<(P > 0 ? P : kMaxRanks)> a)
 {
     using Tr = Traits<T>;
-    using F = Fold<T, OP>;
-    using Acc = typename Tr::Acc;
     constexpr int VEC = Tr::VEC;
     constexpr int S_ELEM = (VEC == 8) ? 2 : 4;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -373,8 +371,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     tma_wide_kernel(const __grid_constant__ TmaArgs<kMaxRanks> a)
 {
     using Tr = Traits<T>;
-    using F = Fold<T, OP>;
-    using Acc = typename Tr::Acc;
     constexpr int VEC = Tr::VEC;
     constexpr int S_ELEM = (VEC == 8) ? 2 : 4;
     extern __shared__ __align__(128) unsigned char smem[];
