@@ -698,3 +698,24 @@ def test_min_max_special_values_follow_compare_and_select(dtype, one, nan, ninf,
     # ring order for p = 2: chunk 0 folds rank 1 then rank 0
     ring = oracle.allreduce([x0, x1], "min", dtype, "ring")[0]
     assert ring[:4].tolist() == [nz, pz, one, nan]
+
+
+def test_special_value_table_holds_what_it_names():
+    """The special-value generator's bit patterns decode (numpy for fp16,
+    torch for bf16) to the values its table names, and draws cover both
+    signs; nan=False leaves NaN out."""
+    import torch
+    f16 = np.array(inputs.SPECIAL_BITS["f16"], dtype=np.uint16).view(np.float16).astype(np.float64)
+    assert f16[:7].tolist() == [0.0, 2.0 ** -24, 1023 * 2.0 ** -24, 2.0 ** -14, 1.0, 1.0 + 2.0 ** -10, 65504.0]
+    assert np.isinf(f16[7]) and np.isnan(f16[8])
+    bits = torch.tensor(np.array(inputs.SPECIAL_BITS["bf16"], dtype=np.uint16).view(np.int16))
+    bf = bits.view(torch.bfloat16).double().numpy()
+    assert bf[:7].tolist() == [0.0, 2.0 ** -133, 127 * 2.0 ** -133, 2.0 ** -126, 1.0, 1.0 + 2.0 ** -7,
+                               (2.0 - 2.0 ** -7) * 2.0 ** 127]
+    assert np.isinf(bf[7]) and np.isnan(bf[8])
+    for dtype in ("f16", "bf16"):
+        d = inputs.specials(4000, 5, 0, dtype)
+        table = set(inputs.SPECIAL_BITS[dtype])
+        assert set(d.tolist()) == table | {b | 0x8000 for b in table}
+        d = inputs.specials(4000, 5, 0, dtype, nan=False)
+        assert not any((b & 0x7FFF) in (0x7E00, 0x7FC0) for b in d.tolist())
