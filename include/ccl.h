@@ -122,7 +122,8 @@ typedef enum {
 typedef enum {
     CCL_VARIANT_AUTO = 0,    /* the ld/st kernel, measured fastest on GB300 with every SM and under budgets
                                 up to 32 SMs; TMA at p <= 8 on half the SMs or more (not all) from
-                                32 MiB per rank, when the layout allows it */
+                                32 MiB per rank, and at p >= 48 on every SM from 64 MiB per rank, when
+                                the layout allows it */
     CCL_VARIANT_LDST = 1,    /* 128-bit register loads/stores, fixed order */
     CCL_VARIANT_TMA = 2,     /* cp.async.bulk into shared-memory stages, fixed order */
     CCL_VARIANT_TMA_BULKRED = 3, /* cp.reduce.async.bulk: order left to the memory system */

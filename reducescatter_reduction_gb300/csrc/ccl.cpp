@@ -207,8 +207,15 @@ extern "C" ccl_schedule_t ccl_select_schedule(int p, double nbytes, const ccl_co
 // (but not all), for 32 MiB per rank and more, where its layout allows it.
 static bool auto_prefers_tma(int p, int sm_budget, int num_sms, double bytes_per_rank)
 {
-    return p <= 8 && sm_budget > 0 && sm_budget < num_sms && 2 * sm_budget >= num_sms &&
-           bytes_per_rank >= 32.0 * 1024 * 1024;
+    const double mib = 1024.0 * 1024.0;
+    // p <= 8 on half the SMs or more (not all): the shared-memory stages hold
+    // more bytes in flight per SM than registers can, from 32 MiB per rank.
+    if (p <= 8 && sm_budget > 0 && sm_budget < num_sms && 2 * sm_budget >= num_sms && bytes_per_rank >= 32.0 * mib)
+        return true;
+    // 48 ranks or more on the whole GPU, from 64 MiB per rank: the wide TMA
+    // kernel edges out the generic ld/st kernel (bf16 p=64 6.95 vs 6.82 TB/s,
+    // p=48 6.92 vs 6.85); at 16 MiB per rank it is 5-8 % behind.
+    return p >= 48 && (sm_budget == 0 || sm_budget >= num_sms) && bytes_per_rank >= 64.0 * mib;
 }
 
 static int resolve_schedule(const ccl_comm *c, int schedule, double nbytes)
@@ -441,7 +448,10 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
             for (int k = 0; k <= p && ok; ++k) ok = (bounds[k] * s) % 16 == 0;
             uint32_t tile, stages;
             size_t smem;
-            if (ok && tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem)) variant = CCL_VARIANT_TMA;
+            uint32_t ranks;
+            const bool fits = p > kTmaNarrowMaxRanks ? tma_wide_geometry(p, c->pipe_bytes, &tile, &ranks, &stages, &smem)
+                                                     : tma_geometry(p, c->pipe_bytes, &tile, &stages, &smem);
+            if (ok && fits) variant = CCL_VARIANT_TMA;
         }
     }
     if ((variant == CCL_VARIANT_RING_STEPWISE || variant == CCL_VARIANT_ONE_PHASE) && coll != COLL_AR)

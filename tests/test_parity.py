@@ -554,7 +554,7 @@ def test_dependent_launch_chain(graph):
 def test_auto_variant_and_budget_kernels():
     """AUTO runs the ld/st kernel, except at p <= 8 on at least half of the SMs
     (not all) for 32 MiB per rank and more, where the TMA variant is measured
-    faster.  Under a budget a large ld/st message runs one 512/1024-thread CTA
+    faster (and at 48 ranks or more, below).  Under a budget a large ld/st message runs one 512/1024-thread CTA
     per SM; a message that already fits in `budget` small CTAs keeps the
     regular kernel."""
     p, n = 16, 16 * 65536                                 # 2 MiB per rank: 131072 groups
@@ -577,6 +577,33 @@ def test_auto_variant_and_budget_kernels():
     _, desc = run_collective([x[: 1 << 23] for x in big], "ar", "sum", "bf16", "ring",
                              variant="auto", budget=half)   # 16 MiB per rank
     assert "variant=ldst" in desc
+
+
+def test_auto_variant_many_ranks():
+    """At 48 ranks and more on the whole GPU AUTO takes the wide TMA kernel
+    from 64 MiB per rank (measured faster there) and the ld/st kernel below;
+    either way the bits equal the ld/st kernel's."""
+    p = 48
+    grain = 8 * p                      # 16-byte chunk boundaries, as the TMA variant needs
+    ins = [torch.empty(34 << 20, dtype=torch.bfloat16, device="cuda").normal_() for _ in range(p)]
+    outs = [torch.empty_like(t) for t in ins]
+    ref = [torch.empty_like(t) for t in ins]
+    h = ccl.ccl_comm_create(p, [t.data_ptr() for t in ins])
+    try:
+        for n, want in (((34 << 20) // grain * grain, "variant=tma"), ((8 << 20) // grain * grain, "variant=ldst")):
+            ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
+            ccl.ccl_set_launch(h, 0, "auto", 0)
+            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", stream_ptr())
+            desc = ccl.ccl_comm_last_launch(h)
+            ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in ref])
+            ccl.ccl_set_launch(h, 0, "ldst", 0)
+            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", stream_ptr())
+            torch.cuda.synchronize()
+            ccl.ccl_comm_check(h)
+            assert want in desc, desc
+            assert all(torch.equal(a[:n].view(torch.int16), b[:n].view(torch.int16)) for a, b in zip(outs, ref))
+    finally:
+        ccl.ccl_comm_destroy(h)
 
 
 def test_largest_buffers_64bit_indexing():
