@@ -1,0 +1,63 @@
+"""Host-side logic of bench.py that decides what its JSON line reports, on
+the CPU: the measured HBM peak and its fallback, DRAM traffic taken from the
+committed ncu summary only while it matches the kernel source, and the
+clock-sample summary with its throttle reasons."""
+import json
+import os
+
+import pytest
+
+import bench
+
+pytestmark = pytest.mark.cpu
+
+
+def test_peak_is_the_measured_copy_bandwidth_else_the_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    peak, src = bench.hbm_peak()
+    assert peak == bench.FALLBACK_HBM_GBS and src.startswith("fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6755.8, "bf16_tflops": 1881.1}))
+    peak, src = bench.hbm_peak()
+    assert peak == 6755.8 and src.startswith("measured")
+
+
+def test_traffic_only_while_the_summary_matches_the_kernel_source(tmp_path, monkeypatch):
+    summary = tmp_path / "summary.md"
+    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(summary))
+    assert bench.profiled_traffic() is None                       # no summary
+    summary.write_text("kernel_source_sha256_16: %s\ndram_bytes_per_launch: 4293472938\n"
+                       % bench.kernel_source_hash())
+    assert bench.profiled_traffic() == 4293472938.0
+    summary.write_text("kernel_source_sha256_16: 0000000000000000\ndram_bytes_per_launch: 4293472938\n")
+    assert bench.profiled_traffic() is None                       # taken on another source
+
+
+def test_committed_summary_names_its_source_and_traffic():
+    text = open(bench.PROFILE_SUMMARY).read()
+    lines = {ln.split(":", 1)[0]: ln.split(":", 1)[1].strip() for ln in text.splitlines() if ":" in ln}
+    assert len(lines["kernel_source_sha256_16"]) == 16
+    traffic = float(lines["dram_bytes_per_launch"])
+    algorithmic = 2 * bench.P * bench.N * bench.S
+    assert 0.99 < traffic / algorithmic < 1.01
+
+
+class _Done:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def test_clock_summary_median_and_reasons(tmp_path):
+    path = tmp_path / "clocks.csv"
+    path.write_text("2070, 2070, 900.1, 0x0000, Not Active, Not Active, Not Active, Not Active\n"
+                    "1965, 2070, 1400.2, 0x0004, Not Active, Not Active, Not Active, Active\n"
+                    "2070, 2070, 1100.0, 0x0000, Not Active, Not Active, Not Active, Not Active\n"
+                    "[N/A], 2070, 0, 0, x, x, x, x\n")
+    s = bench.ClockSampler(None)
+    s.proc = _Done()
+    s.file = open(path, "r+")
+    out = s.stop()
+    assert out == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
+    assert not os.path.exists(path)
