@@ -71,6 +71,9 @@ def parse_args(argv=None):
     ap.add_argument("--moe-rows", type=int, default=0,
                     help="profiling mode: only the p=16 bf16 [rows, 7168] ring AllReduce with --variant and "
                          "--sm-budget, warmup + steps calls")
+    ap.add_argument("--host-buffers", action="store_true",
+                    help="profiling mode: only the zero-copy AllReduce, p=8 bf16 rank buffers of --n elements in "
+                         "pinned host memory (inputs and outputs), --sm-budget, warmup + steps calls")
     ap.add_argument("--calibrate", action="store_true",
                     help="fit t = alpha + bytes/B per variant and SM budget (p=8 bf16) and print the table")
     ap.add_argument("--n", type=int, default=N,
@@ -1066,6 +1069,38 @@ def main(argv=None):
         print(json.dumps({"mode": "moe", "rows": args.moe_rows, "variant": args.variant,
                           "sm_budget": args.sm_budget, "us_per_call": round(us, 2),
                           "GBps": round(2 * p * n * S / (us * 1e-6) / 1e9, 1),
+                          "launch": ccl.ccl_comm_last_launch(h)}), flush=True)
+        ccl.ccl_comm_destroy(h)
+        return 0
+    if args.host_buffers:
+        import torch
+        import __graft_entry__
+        import reducescatter_reduction_gb300 as ccl
+        __graft_entry__.build()
+        dev = torch.device("cuda", dist.local_rank)
+        torch.cuda.set_device(dev)
+        n = args.n
+        ins = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
+        for t in ins:
+            t.copy_(torch.randn(n, device=dev).to(torch.bfloat16))
+        outs = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(P)]
+        h = ccl.ccl_comm_create(P, [t.data_ptr() for t in ins])
+        ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
+        ccl.ccl_set_launch(h, args.sm_budget, "ldst", 0)
+        s = torch.cuda.current_stream()
+        for _ in range(args.warmup):
+            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s.cuda_stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s.cuda_stream)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / max(1, args.steps)
+        ccl.ccl_comm_check(h)
+        print(json.dumps({"mode": "host_buffers", "n_per_rank": n, "sm_budget": args.sm_budget,
+                          "us_per_call": round(us, 2), "GBps": round(2 * P * n * S / (us * 1e-6) / 1e9, 1),
                           "launch": ccl.ccl_comm_last_launch(h)}), flush=True)
         ccl.ccl_comm_destroy(h)
         return 0
