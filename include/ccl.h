@@ -1,14 +1,15 @@
 /*
  * ccl.h -- AllReduce, ReduceScatter and AllGather over p "rank" buffers that
- * all live in the memory of one GPU (NVIDIA GB300, sm_103a).
+ * all live in the memory of one GPU (NVIDIA GB300, sm_103a), or in pinned
+ * host memory that GPU addresses directly.
  *
  * What is computed.  "Inside NCCL AllReduce", section "What all-reduce
  * promises": all-reduce combines one same-shaped buffer per rank element by
  * element (sum, prod, min, max or avg), and at the end all ranks hold the same
  * result; it equals a reduce-scatter (each rank ends owning the
  * finished reduction of one slice) followed by an all-gather (the finished
- * slices go to every rank).  Here the p ranks are p device buffers; there
- * are no peer GPUs and no messages.  Each element is reduced once, in fp32
+ * slices go to every rank).  Here the p ranks are p buffers one GPU
+ * addresses; there are no peer GPUs and no messages.  Each element is reduced once, in fp32
  * for floating-point types (int32 for int32), in the exact rank order that
  * the schedule gives its chunk, and the finished value is written to every
  * destination in the same pass.
@@ -44,8 +45,8 @@
  * to |err| <= 2 * p * eps(element type) * sum_k |x_k| per element instead (its
  * min/max pick the same value, but which of +0 and -0, or which NaN, is not
  * fixed); the stepwise-ring executor rounds each partial to the element type
- * at every hop (see ccl_variant_t).  A NaN that min/max keep is the input's
- * own bit pattern for fp16/bf16.
+ * at every hop (see ccl_variant_t).  A NaN that the ld/st or TMA variants'
+ * min/max keep is the input's own bit pattern for fp16/bf16.
  *
  * Memory and ownership.  The caller allocates and owns every rank buffer
  * (device memory, e.g. from PyTorch).  A communicator copies the p input and
