@@ -61,3 +61,22 @@ def test_clock_summary_median_and_reasons(tmp_path):
     out = s.stop()
     assert out == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
     assert not os.path.exists(path)
+
+
+def test_workload_recipe_matches_the_benchmark():
+    """The seeded workloads have the shapes the benchmark and the parity tests
+    name: the p=8 bf16 sweep up to 2^27 elements (256 MiB) per rank, TP
+    activations of hidden 8192 at 1/32/256/4096 tokens, the 64 Mi-element op
+    coverage set, the p=16 [16384, 7168] MoE buffers; every workload its own
+    seed."""
+    from reducescatter_reduction_gb300 import inputs
+    assert inputs.SWEEP_N[0] * 2 == 1024 and inputs.SWEEP_N[-1] == bench.N == 1 << 27
+    assert bench.P == 8 and bench.S == inputs.ELEM_BYTES["bf16"]
+    assert inputs.TP_HIDDEN == 8192 and inputs.TP_TOKENS == [1, 32, 256, 4096]
+    assert inputs.COVERAGE_N == 64 * 1024 * 1024
+    assert inputs.MOE_SHAPE == (16384, 7168)
+    assert len(set(inputs.SEEDS.values())) == len(inputs.SEEDS)
+    a = inputs.normal(1000, inputs.SEEDS["sweep"], 3, 1.0, "bf16")
+    b = inputs.normal(1000, inputs.SEEDS["sweep"], 3, 1.0, "bf16")
+    c = inputs.normal(1000, inputs.SEEDS["sweep"], 4, 1.0, "bf16")
+    assert (a == b).all() and not (a == c).all()                  # seeded per (workload, rank)
