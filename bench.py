@@ -10,10 +10,10 @@ AllReduce in which every rank receives the result: p*n*s read + p*n*s written.
 Printed JSON line (rank 0): value = whole-job GB/s over K timed steps (CUDA
 events on the launching stream, barrier + synchronize on both sides, max over
 ranks), plus roofline (the fused kernel against the measured HBM copy peak),
-e2e (same metric with host buffers: pinned H2D copy, AllReduce, D2H copy
-inside the timed region), the CPU oracle baseline, clocks sampled during the
-timed region, and the message-size sweep (1 KiB .. 256 MiB per rank, ring and
-all-pairs).
+e2e (same metric with pinned host buffers, every byte crossing the host link
+inside the timed region: the kernel on the host buffers, or staged copies),
+the CPU oracle baseline, clocks sampled during the timed region, and the
+message-size sweep (1 KiB .. 256 MiB per rank, ring and all-pairs).
 
 Multi-GPU: one process per GPU (torchrun), each an independent replica of the
 workload (the collective's p ranks are buffers in one GPU's memory; there is
