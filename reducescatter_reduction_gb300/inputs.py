@@ -24,6 +24,22 @@ coverage      p=8, n = 64 Mi; int32 uniform in [-1000, 1000] (prod: values  4
               from {-1, 1, 2}); fp32 / fp16 N(0, 1)
 moe           p=16 bf16, [16384, 7168] per rank, N(0, 1)                 5
 ============  =========================================================  ======
+
+Parity-only recipes whose results depend on the rank order of every chunk,
+so that a test comparing bits also checks the order (N(0,1) at bf16 or fp16
+hides it: the fp32 sum of a few such values is almost always exact):
+
+- ``cancel``: at each element two ranks (the same draw for every rank) hold
+  +B and -B, B a large number with a random significand; every other rank
+  holds a small normal value.  Whether a small value still counts in the
+  result depends on where it falls relative to the two large ones.
+- ``signed_zero``: +0 everywhere except that rank e mod p holds -0 at element
+  e; min and max keep whichever zero they meet first.
+- ``prod_inexact``: random signs times uniform values in [0.75, 1.3), whose
+  products are inexact in fp32 and in the element type.
+- ``prod_overflow``: at each element two ranks hold about 2^100 and one
+  holds about 2^-100, the rest values near 1; some orders take the fp32
+  product past the largest finite value, others never.  bf16 and fp32 only.
 """
 from __future__ import annotations
 
@@ -137,3 +153,67 @@ def coverage(op: str, dtype: str, n: int = COVERAGE_N, p: int = 8):
 def moe(p: int = 16, shape=MOE_SHAPE, dtype: str = "bf16"):
     n = shape[0] * shape[1]
     return [normal(n, SEEDS["moe"], r, 1.0, dtype) for r in range(p)]
+
+
+# ---------------------------------------------------------------------------
+# order-revealing parity inputs (see the module docstring)
+# ---------------------------------------------------------------------------
+
+_LAYOUT_RANK = 1 << 20   # the stream shared by every rank of a workload (element placement)
+
+
+def _two_ranks(n: int, seed: int, p: int):
+    """Per element, two distinct ranks j != m, drawn from the shared stream."""
+    g = rng(seed, _LAYOUT_RANK)
+    j = g.integers(0, p, size=n)
+    m = (j + 1 + g.integers(0, max(p - 1, 1), size=n)) % p
+    return g, j, m
+
+
+def cancel(n: int, seed: int, rank: int, p: int, dtype: str) -> np.ndarray:
+    big_exp, small_scale = (14, 0.25) if dtype == "f16" else (24, 1.0)
+    g, j, m = _two_ranks(n, seed, p)
+    big = (1.0 + g.random(n, dtype=np.float32)) * np.float32(2.0 ** big_exp)
+    v = rng(seed, rank).standard_normal(n, dtype=np.float32) * np.float32(small_scale)
+    v = np.where(j == rank, big, np.where(m == rank, -big, v)).astype(np.float32)
+    return store(v, dtype)
+
+
+def cancel_ranks(n: int, seed: int, p: int, dtype: str):
+    """All p ranks of ``cancel`` at once (the same arrays, the layout drawn once)."""
+    big_exp, small_scale = (14, 0.25) if dtype == "f16" else (24, 1.0)
+    g, j, m = _two_ranks(n, seed, p)
+    big = (1.0 + g.random(n, dtype=np.float32)) * np.float32(2.0 ** big_exp)
+    out = []
+    for r in range(p):
+        v = rng(seed, r).standard_normal(n, dtype=np.float32) * np.float32(small_scale)
+        v[j == r] = big[j == r]
+        v[m == r] = -big[m == r]
+        out.append(store(v, dtype))
+    return out
+
+
+def signed_zero(n: int, rank: int, p: int, dtype: str) -> np.ndarray:
+    v = np.zeros(n, dtype=np.float32)
+    v[(np.arange(n) % p) == rank] = -0.0
+    return store(v, dtype)
+
+
+def prod_inexact(n: int, seed: int, rank: int, dtype: str) -> np.ndarray:
+    g = rng(seed, rank)
+    mag = np.float32(0.75) + np.float32(0.55) * g.random(n, dtype=np.float32)
+    sign = np.where(g.random(n) < 0.5, np.float32(-1.0), np.float32(1.0))
+    return store((mag * sign).astype(np.float32), dtype)
+
+
+def prod_overflow(n: int, seed: int, rank: int, p: int, dtype: str) -> np.ndarray:
+    if dtype not in ("f32", "bf16"):
+        raise ValueError("prod_overflow needs the fp32 exponent range (f32 or bf16)")
+    g, j, m = _two_ranks(n, seed, p)
+    i = (m + 1 + g.integers(0, max(p - 2, 1), size=n)) % p   # a third rank: i != m
+    i = np.where(i == j, (i + 1) % p, i)                       # ... and i != j when p > 2
+    big = (1.0 + g.random(n, dtype=np.float32)) * np.float32(2.0 ** 100)
+    tiny = (1.0 + g.random(n, dtype=np.float32)) * np.float32(2.0 ** -100)
+    v = prod_inexact(n, seed, rank, "f32")
+    v = np.where((j == rank) | (m == rank), big, np.where(i == rank, tiny, v)).astype(np.float32)
+    return store(v, dtype)
