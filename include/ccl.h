@@ -28,8 +28,16 @@
  *  - CCL_SCHED_AUTO: the alpha-beta cost model of "MSCCL, in depth" (sections
  *    "Why generic collectives leave time on the table" and "Worked example:
  *    all-pairs versus ring on 8 GPUs") picks ring or all-pairs; see
- *    ccl_select_schedule().  The environment variable CCL_SCHEDULE=ring|allpairs
- *    overrides AUTO only.
+ *    ccl_select_schedule().
+ *
+ * Environment overrides, as NCCL's NCCL_ALGO and NCCL_PROTO: CCL_SCHEDULE=
+ * ring|allpairs|auto, CCL_VARIANT=ldst|tma|tma_bulkred|auto and
+ * CCL_SM_BUDGET=<k> apply only where the choice is left open -- schedule
+ * CCL_SCHED_AUTO in the call, variant CCL_VARIANT_AUTO and SM budget 0 in the
+ * communicator (ccl_set_launch); explicit values win.  CCL_VARIANT does not
+ * apply to AllGather, which has one kernel.  An unset or empty variable
+ * changes nothing; any other value outside these lists makes the call fail
+ * with CCL_ERR_INVALID_ARG.
  *
  * Numerics.  fp16/bf16/fp32 inputs are widened exactly to fp32; partial
  * results stay fp32 for all p-1 steps; the result is rounded once to the
@@ -157,8 +165,14 @@ typedef enum {
 CCL_API ccl_status_t ccl_comm_create(ccl_comm_t *out, int p, void *const *rank_ptrs);
 
 /* Set the p output buffers (host array of device pointers, copied).  NULL
- * restores in-place operation (outputs = inputs).  Aliasing is checked at
- * each call, since only then are sizes known. */
+ * restores in-place operation (outputs = inputs).  T-CCL, section
+ * "Programming Model": each rank passes its own buffer, and both in-place and
+ * out-of-place operation are supported, as in NCCL.  In place means
+ * out_ptrs[r] == rank_ptrs[r] for AllReduce and AllGather, and out_ptrs[r] ==
+ * rank_ptrs[r] + r*n/p elements for ReduceScatter (NCCL's convention); any
+ * other overlap is refused.  Aliasing is checked at each call, since only
+ * then are sizes known.  Errors: CCL_ERR_INVALID_ARG (NULL comm, a NULL
+ * output pointer). */
 CCL_API ccl_status_t ccl_comm_set_outputs(ccl_comm_t comm, void *const *out_ptrs);
 
 /* Set the per-chunk accumulation orders used by CCL_SCHED_CUSTOM.
@@ -200,12 +214,14 @@ CCL_API ccl_status_t ccl_set_launch(ccl_comm_t comm, int sm_budget, int variant,
  * Errors: CCL_ERR_INVALID_ARG for negative values or stall_test > 1. */
 CCL_API ccl_status_t ccl_comm_set_debug(ccl_comm_t comm, long long wait_limit_ns, int stall_test);
 
-/* Release the communicator and its device status block.  Waits for
- * nothing: the caller must not destroy a communicator whose kernels are
- * still in flight.  NULL is accepted. */
+/* Release the communicator and its device status block (no passage of the
+ * pages: housekeeping).  Waits for nothing: the caller must not destroy a
+ * communicator whose kernels are still in flight.  NULL is accepted.
+ * Errors: CCL_ERR_CUDA if freeing the status block fails. */
 CCL_API ccl_status_t ccl_comm_destroy(ccl_comm_t comm);
 
-/* Synchronise the communicator's device and read its status block.
+/* Synchronise the communicator's device and read its status block (no
+ * passage of the pages: failure detection, housekeeping).
  * CCL_ERR_TIMEOUT if a bounded wait in a kernel gave up since the last
  * check (the block is then cleared), CCL_ERR_CUDA on a CUDA error,
  * otherwise CCL_OK. */
@@ -215,7 +231,11 @@ CCL_API ccl_status_t ccl_comm_check(ccl_comm_t comm);
  * Collectives.  n is always the element count of one full rank buffer.
  * ------------------------------------------------------------------------- */
 
-/* AllReduce: out[r][e] = reduction over ranks of in[k][e], for every r and
+/* AllReduce ("Inside NCCL AllReduce", section "What all-reduce promises":
+ * every rank ends with the same element-wise reduction of all p buffers; the
+ * ring of "The ring, exactly as the kernel runs it" and the all-pairs program
+ * of "MSCCL, in depth", "Writing an algorithm in MSCCLang", fix the order):
+ * out[r][e] = reduction over ranks of in[k][e], for every r and
  * every e < n, each chunk in its schedule order.  In place (out[r] ==
  * in[r]) or out of place; any other overlap between an output and any
  * buffer is CCL_ERR_INVALID_ARG.  Any n >= 0 (n == 0 is a no-op).
@@ -223,7 +243,10 @@ CCL_API ccl_status_t ccl_comm_check(ccl_comm_t comm);
 CCL_API ccl_status_t ccl_allreduce(ccl_comm_t comm, ccl_op_t op, ccl_dtype_t dtype, size_t n,
                            ccl_schedule_t schedule, void *stream);
 
-/* ReduceScatter: out[r][i] = element c_r + i of the reduction, 0 <= i < n/p,
+/* ReduceScatter ("Inside NCCL AllReduce", "What all-reduce promises": each
+ * rank ends owning the finished reduction of one slice; T-CCL, "Shard
+ * Ownership": the owner of a shard produces its final value):
+ * out[r][i] = element c_r + i of the reduction, 0 <= i < n/p,
  * where c_r = r*n/p: rank r receives its own chunk, written from offset 0.
  * Requires n % p == 0 (else CCL_ERR_INVALID_ARG, never a silent fallback).
  * In place in NCCL's sense (out[r] == in[r] + r*n/p elements) or disjoint.
@@ -231,7 +254,10 @@ CCL_API ccl_status_t ccl_allreduce(ccl_comm_t comm, ccl_op_t op, ccl_dtype_t dty
 CCL_API ccl_status_t ccl_reduce_scatter(ccl_comm_t comm, ccl_op_t op, ccl_dtype_t dtype, size_t n,
                                 ccl_schedule_t schedule, void *stream);
 
-/* AllGather: rank r contributes elements [r*n/p, (r+1)*n/p) of its input
+/* AllGather ("Inside NCCL AllReduce", "The ring, exactly as the kernel runs
+ * it": in the all-gather half the finished chunks travel unchanged to every
+ * rank; T-CCL, "Chunk and Window Decomposition": one load fanned out to every
+ * destination): rank r contributes elements [r*n/p, (r+1)*n/p) of its input
  * buffer in[r] (n elements); every rank's output out[k] receives all n
  * elements, rank r's chunk at offset r*n/p.  Requires n % p == 0.  In place
  * (out[k] == in[k]: the owner's own chunk is not rewritten) or disjoint.
@@ -263,10 +289,10 @@ CCL_API ccl_status_t ccl_allreduce_residual_rmsnorm(ccl_comm_t comm, ccl_dtype_t
 /* AllReduce for callers that cannot allocate device memory.  The pages have
  * no counterpart: this entry point exists for code that may not call
  * cudaMalloc -- a plug-in inside an application that owns all device memory
- * (an inference server, a framework's memory pool), a process whose memory
- * budget is already committed, or a latency-critical path that cannot afford
- * cudaMalloc's implicit device synchronisation or its failure under memory
- * pressure.  It needs no communicator and allocates nothing: no cudaMalloc, no
+ * and hands out only the buffers it manages (an inference server, a
+ * framework's memory pool), a process whose memory budget is already
+ * committed, or code that must not meet an out-of-memory failure once it is
+ * running.  It needs no communicator and allocates nothing: no cudaMalloc, no
  * cudaFree, no allocating library routine.
  *
  * Computes exactly what ccl_allreduce computes (same chunks, same orders, same
@@ -286,15 +312,25 @@ CCL_API ccl_status_t ccl_allreduce_residual_rmsnorm(ccl_comm_t comm, ccl_dtype_t
  * the library holds until the process exits.  The first call on a device looks
  * up that array's device address; make that first call before any stream
  * capture.  All calls share the array and it keeps the last call's contents:
- * each call first waits for the work already queued on `stream`, reads the
- * record the previous call left (returning CCL_ERR_TIMEOUT, without
- * launching, if a wait of that call gave up -- its outputs are then
- * incomplete), then clears it.  Calls that overlap on the GPU (other streams,
- * other threads) race on the record.
+ * each call first waits for the work already queued on `stream` -- the
+ * calling host thread blocks until that work is done -- and reads the record
+ * the previous call left (returning CCL_ERR_TIMEOUT, without launching, if a
+ * wait of that call gave up -- its outputs are then incomplete), then clears
+ * it.  Calls that overlap on the GPU (other streams, other threads) race on
+ * the record.
  * Errors: CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED, CCL_ERR_TIMEOUT,
  * CCL_ERR_CUDA; messages through ccl_last_error(). */
 CCL_API ccl_status_t ccl_allreduce_static(int p, void *const *in_ptrs, void *const *out_ptrs, ccl_op_t op,
                                           ccl_dtype_t dtype, size_t n, ccl_schedule_t schedule, void *stream);
+
+/* Failure-detection hook of ccl_allreduce_static (tests); no passage of the
+ * pages: housekeeping.  Sets, for every later call in this process, the bound
+ * on any single wait of its kernel (0 restores the default of 2 s) and
+ * whether its producer withholds the second tile (stall_test = 1), so that a
+ * wait runs out on purpose and the next call reports CCL_ERR_TIMEOUT.
+ * Nothing traps or faults.  Errors: CCL_ERR_INVALID_ARG for negative values
+ * or stall_test > 1. */
+CCL_API ccl_status_t ccl_allreduce_static_set_debug(long long wait_limit_ns, int stall_test);
 
 /* ---------------------------------------------------------------------------
  * Host-side schedule builder and cost model (no GPU needed).
@@ -338,19 +374,27 @@ CCL_API ccl_schedule_t ccl_select_schedule(int p, double nbytes, const ccl_cost_
  * Diagnostics.
  * ------------------------------------------------------------------------- */
 
-/* Message for the last non-OK status returned on this host thread. */
+/* Message for the last non-OK status returned on this host thread (no
+ * passage of the pages: housekeeping).  Never NULL; the string is owned by
+ * the library and valid until the next call on this thread. */
 CCL_API const char *ccl_last_error(void);
 
 /* Description of the last kernel launch this communicator issued (kernel,
- * dtype, op, p, n, schedule, variant, grid, block, shared memory), so that
- * a caller can prove which path ran.  Copies at most len-1 characters plus
- * a terminating NUL into buf; returns CCL_ERR_INVALID_ARG if buf is NULL. */
+ * dtype, op, p, n, schedule, variant, grid, block, shared memory, SM budget,
+ * counter=1 when CTAs or warps took work from a device-wide counter, and
+ * inplace=1 when an output is an input, so that the kernels loaded without
+ * ld.global.nc), so
+ * that a caller can prove which path ran -- "MSCCL, in depth", section
+ * "Deploying it": check that the custom algorithm actually ran instead of a
+ * silent fallback.  Copies at most len-1 characters plus a terminating NUL
+ * into buf; returns CCL_ERR_INVALID_ARG if comm or buf is NULL or len is 0. */
 CCL_API ccl_status_t ccl_comm_last_launch(ccl_comm_t comm, char *buf, size_t len);
 
-/* Number of kernels this communicator has launched since creation. */
+/* Number of kernels this communicator has launched since creation (no
+ * passage of the pages: housekeeping; 0 for a NULL comm). */
 CCL_API uint64_t ccl_comm_launch_count(ccl_comm_t comm);
 
-/* CCL_VERSION of the loaded library. */
+/* CCL_VERSION of the loaded library (housekeeping). */
 CCL_API int ccl_version(void);
 
 #ifdef __cplusplus

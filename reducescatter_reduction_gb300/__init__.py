@@ -43,7 +43,7 @@ STATUS_NAMES = {CCL_OK: "CCL_OK", CCL_ERR_INVALID_ARG: "CCL_ERR_INVALID_ARG",
 EXPORTS = (
     "ccl_comm_create", "ccl_comm_set_outputs", "ccl_comm_set_schedule", "ccl_set_launch", "ccl_comm_set_debug",
     "ccl_comm_destroy", "ccl_comm_check", "ccl_allreduce", "ccl_reduce_scatter", "ccl_all_gather",
-    "ccl_allreduce_static", "ccl_allreduce_residual_rmsnorm",
+    "ccl_allreduce_static", "ccl_allreduce_static_set_debug", "ccl_allreduce_residual_rmsnorm",
     "ccl_schedule_build", "ccl_schedule_check", "ccl_cost_estimate", "ccl_select_schedule",
     "ccl_last_error", "ccl_comm_last_launch", "ccl_comm_launch_count", "ccl_version",
 )
@@ -86,6 +86,7 @@ def load_library(path: str = LIB_PATH):
         "ccl_reduce_scatter": (i, [vp, i, i, sz, i, vp]),
         "ccl_all_gather": (i, [vp, i, sz, vp]),
         "ccl_allreduce_static": (i, [i, pvp, pvp, i, i, sz, i, vp]),
+        "ccl_allreduce_static_set_debug": (i, [ctypes.c_longlong, i]),
         "ccl_allreduce_residual_rmsnorm": (i, [vp, i, sz, sz, vp, vp, vp, ctypes.c_float, i, vp]),
         "ccl_schedule_build": (i, [i, u64, i, ctypes.POINTER(u64), ctypes.POINTER(ctypes.c_uint8)]),
         "ccl_schedule_check": (i, [i, u64, ctypes.POINTER(u64), ctypes.POINTER(ctypes.c_uint8)]),
@@ -193,6 +194,10 @@ def ccl_allreduce_static(p: int, in_ptrs, out_ptrs, op, dtype, n: int, schedule=
     _check(load_library().ccl_allreduce_static(int(p), _ptr_array(in_ptrs), _ptr_array(out_ptrs),
                                                _code(OPS, op), _code(DTYPES, dtype), int(n),
                                                _code(SCHEDULES, schedule), stream or None))
+
+
+def ccl_allreduce_static_set_debug(wait_limit_ns: int = 0, stall_test: int = 0) -> None:
+    _check(load_library().ccl_allreduce_static_set_debug(int(wait_limit_ns), int(stall_test)))
 
 
 def ccl_allreduce_residual_rmsnorm(comm: int, dtype, rows: int, hidden: int, residual_in: int,

@@ -264,6 +264,7 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
         info->block = block;
         info->smem = smem;
         info->kernels = 1;
+        info->counter = a.dynamic;
     }
     return cudaGetLastError();
 }

@@ -218,12 +218,52 @@ static bool auto_prefers_tma(int p, int sm_budget, int num_sms, double bytes_per
     return p >= 48 && (sm_budget == 0 || sm_budget >= num_sms) && bytes_per_rank >= 64.0 * mib;
 }
 
+// Environment overrides, as NCCL's NCCL_ALGO / NCCL_PROTO ("Inside NCCL
+// AllReduce", section on the tuner): CCL_SCHEDULE=ring|allpairs|auto,
+// CCL_VARIANT=ldst|tma|tma_bulkred|auto and CCL_SM_BUDGET=<k> apply only where
+// the call or the communicator left the choice open (schedule AUTO, variant
+// AUTO, SM budget 0).  An unset or empty variable changes nothing; any other
+// value that is not one of the listed ones is an error, never ignored.
+static bool env_schedule(int *out)
+{
+    const char *e = getenv("CCL_SCHEDULE");
+    if (!e || !*e || strcmp(e, "auto") == 0) return true;
+    if (strcmp(e, "ring") == 0) *out = CCL_SCHED_RING;
+    else if (strcmp(e, "allpairs") == 0) *out = CCL_SCHED_ALLPAIRS;
+    else return false;
+    return true;
+}
+
+static bool env_variant(int *out)
+{
+    const char *e = getenv("CCL_VARIANT");
+    if (!e || !*e || strcmp(e, "auto") == 0) return true;
+    if (strcmp(e, "ldst") == 0) *out = CCL_VARIANT_LDST;
+    else if (strcmp(e, "tma") == 0) *out = CCL_VARIANT_TMA;
+    else if (strcmp(e, "tma_bulkred") == 0) *out = CCL_VARIANT_TMA_BULKRED;
+    else return false;
+    return true;
+}
+
+static bool env_sm_budget(int *out)
+{
+    const char *e = getenv("CCL_SM_BUDGET");
+    if (!e || !*e) return true;
+    char *end = nullptr;
+    const long v = strtol(e, &end, 10);
+    if (*end != '\0' || v < 0 || v > 1000000) return false;
+    *out = int(v);
+    return true;
+}
+
+// schedule AUTO: CCL_SCHEDULE if set, else the cost model.  -1 if the
+// variable holds something else.
 static int resolve_schedule(const ccl_comm *c, int schedule, double nbytes)
 {
     if (schedule != CCL_SCHED_AUTO) return schedule;
-    const char *e = getenv("CCL_SCHEDULE");
-    if (e && strcmp(e, "ring") == 0) return CCL_SCHED_RING;
-    if (e && strcmp(e, "allpairs") == 0) return CCL_SCHED_ALLPAIRS;
+    int s = CCL_SCHED_AUTO;
+    if (!env_schedule(&s)) return -1;
+    if (s != CCL_SCHED_AUTO) return s;
     return ccl_select_schedule(c->p, nbytes, nullptr);
 }
 
@@ -388,7 +428,10 @@ static bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.l
 // any rank reads, except the exact in-place alias of its own rank:
 //   AR: out[r] == in[r];  RS: out[r] == in[r] + chunk r;  AG: out[r] == in[r].
 // With those aliases each element is read and written by one thread only.
-static ccl_status_t check_aliases(const ccl_comm *c, int coll, uint64_t n, size_t s, uint64_t *self_mask)
+// *alias is set when an output is (part of) an input: the kernels then load
+// with coherent loads instead of ld.global.nc.
+static ccl_status_t check_aliases(const ccl_comm *c, int coll, uint64_t n, size_t s, uint64_t *self_mask,
+                                  bool *alias = nullptr)
 {
     const int p = c->p;
     const uint64_t chunk = n / uint64_t(p);
@@ -401,6 +444,7 @@ static ccl_status_t check_aliases(const ccl_comm *c, int coll, uint64_t n, size_
         else wr[r] = {out, out + n * s};
     }
     *self_mask = 0;
+    if (alias) *alias = false;
     for (int k = 0; k < p; ++k) {
         for (int j = k + 1; j < p; ++j)
             if (overlap(wr[k], wr[j])) return fail(CCL_ERR_INVALID_ARG, "outputs of ranks %d and %d overlap", k, j);
@@ -414,6 +458,7 @@ static ccl_status_t check_aliases(const ccl_comm *c, int coll, uint64_t n, size_
             }
             if (!ok) return fail(CCL_ERR_INVALID_ARG, "output of rank %d overlaps the input of rank %d", k, j);
             if (coll == COLL_AG) *self_mask |= uint64_t(1) << k;
+            if (alias) *alias = true;
         }
     }
     return CCL_OK;
@@ -433,13 +478,18 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     if (coll != COLL_AR && n % size_t(p) != 0)
         return fail(CCL_ERR_INVALID_ARG, "%s needs n %% p == 0 (n=%zu, p=%d)", kCollName[coll], n, p);
     if (n > (SIZE_MAX / 2) / s) return fail(CCL_ERR_INVALID_ARG, "n=%zu too large", n);
-    // AUTO: the ld/st kernel, or the TMA variant where auto_prefers_tma says
-    // it is measured faster and the layout allows it.  AllGather has only the
-    // ld/st kernel.
+    int sm_budget = c->sm_budget;
+    if (sm_budget == 0 && !env_sm_budget(&sm_budget))
+        return fail(CCL_ERR_INVALID_ARG, "CCL_SM_BUDGET=%s is not a count of SMs", getenv("CCL_SM_BUDGET"));
+    // AUTO: CCL_VARIANT if set; else the ld/st kernel, or the TMA variant
+    // where auto_prefers_tma says it is measured faster and the layout allows
+    // it.  AllGather has only the ld/st kernel.
     int variant = c->variant;
+    if (variant == CCL_VARIANT_AUTO && coll != COLL_AG && !env_variant(&variant))
+        return fail(CCL_ERR_INVALID_ARG, "CCL_VARIANT=%s is not ldst, tma, tma_bulkred or auto", getenv("CCL_VARIANT"));
     if (variant == CCL_VARIANT_AUTO) {
         variant = CCL_VARIANT_LDST;
-        if (coll != COLL_AG && n > 0 && auto_prefers_tma(p, c->sm_budget, c->num_sms, double(n) * double(s))) {
+        if (coll != COLL_AG && n > 0 && auto_prefers_tma(p, sm_budget, c->num_sms, double(n) * double(s))) {
             uint64_t bounds[kMaxRanks + 1];
             chunk_bounds(p, n, bounds);
             bool ok = true;
@@ -468,7 +518,8 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     if (n == 0) return CCL_OK;
 
     uint64_t self_mask = 0;
-    ccl_status_t st = check_aliases(c, coll, n, s, &self_mask);
+    bool alias = false;
+    ccl_status_t st = check_aliases(c, coll, n, s, &self_mask, &alias);
     if (st != CCL_OK) return st;
     if (variant == CCL_VARIANT_ONE_PHASE)
         for (int r = 0; r < p; ++r)
@@ -492,9 +543,10 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     }
     L.vec = aligned && (coll == COLL_AR || (n / p * s) % 16 == 0);
     L.self_mask = self_mask;
+    L.alias = alias;
     L.device = c->device;
     L.num_sms = c->num_sms;
-    L.sm_budget = c->sm_budget;
+    L.sm_budget = sm_budget;
     L.pipe_bytes = c->pipe_bytes;
     L.status = c->d_status;
     L.wait_limit_ns = c->wait_limit_ns;
@@ -505,6 +557,8 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     if (coll != COLL_AG) {
         sched = variant == CCL_VARIANT_RING_STEPWISE ? int(CCL_SCHED_RING)
                                                      : resolve_schedule(c, schedule, double(n) * double(s));
+        if (sched < 0)
+            return fail(CCL_ERR_INVALID_ARG, "CCL_SCHEDULE=%s is not ring, allpairs or auto", getenv("CCL_SCHEDULE"));
         L.table = get_table(c, n, sched);
     }
     if (variant == CCL_VARIANT_RING_STEPWISE || variant == CCL_VARIANT_ONE_PHASE) {
@@ -581,10 +635,11 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     }
     c->launches += uint64_t(info.kernels);
     snprintf(c->last, sizeof c->last,
-             "%s dtype=%s op=%s p=%d n=%zu schedule=%s variant=%s vec=%d grid=%d block=%d smem=%zu sm_budget=%d",
+             "%s dtype=%s op=%s p=%d n=%zu schedule=%s variant=%s vec=%d grid=%d block=%d smem=%zu sm_budget=%d "
+             "counter=%d inplace=%d",
              info.kernel, kDtypeName[dtype], coll == COLL_AG ? "copy" : kOpName[op], p, n,
              coll == COLL_AG ? "-" : kSchedName[sched], kVariantName[variant], L.vec ? 1 : 0, info.grid, info.block,
-             info.smem, c->sm_budget);
+             info.smem, sm_budget, info.counter, alias ? 1 : 0);
     if (debug_on()) fprintf(stderr, "[ccl] %s\n", c->last);
     if (err != cudaSuccess) return cuda_fail(err, kCollName[coll]);
     return CCL_OK;
@@ -663,6 +718,8 @@ extern "C" ccl_status_t ccl_allreduce_residual_rmsnorm(ccl_comm_t c, ccl_dtype_t
     L.num_sms = c->num_sms;
     L.stream = static_cast<cudaStream_t>(stream);
     const int sched = resolve_schedule(c, schedule, double(n) * double(s));
+    if (sched < 0)
+        return fail(CCL_ERR_INVALID_ARG, "CCL_SCHEDULE=%s is not ring, allpairs or auto", getenv("CCL_SCHEDULE"));
     L.table = get_table(c, n, sched);
     for (int k = 0; k <= p && aligned; ++k) aligned = L.table->bound[k] % vec_elems == 0;
     L.vec = aligned;

@@ -16,6 +16,9 @@
 // reads every peer's data and reduces all of it itself): each rank's output is
 // computed independently from all p inputs, in the chunk's order -- the fused
 // kernel's bits with p times its reads (p^2 n s read + p n s written).
+//
+// Loads are coherent (no ld.global.nc): in place, a reduce-scatter hop reads
+// a rank's contribution and overwrites it with the partial.
 #include "device.cuh"
 
 namespace ccl {
@@ -85,14 +88,14 @@ __global__ void __launch_bounds__(kCmpThreads) ring_rs_hop_kernel(const __grid_c
         const int d = (c + 1 + h) % p;
         Acc held[VEC], v[VEC];
         if (h == 1) {
-            Tr::unpack(ld_stream_v4(static_cast<const char *>(a.src[(c + 1) % p]) + e * S), v);
+            Tr::unpack(ld_coherent_v4(static_cast<const char *>(a.src[(c + 1) % p]) + e * S), v);
 #pragma unroll
             for (int i = 0; i < VEC; ++i) v[i] = F::first(v[i], a.scale);
             Tr::unpack(Tr::pack(v), held);              // held in the element type
         } else {
-            Tr::unpack(ld_stream_v4(static_cast<const char *>(a.dst[(c + h) % p]) + e * S), held);
+            Tr::unpack(ld_coherent_v4(static_cast<const char *>(a.dst[(c + h) % p]) + e * S), held);
         }
-        Tr::unpack(ld_stream_v4(static_cast<const char *>(a.src[d]) + e * S), v);
+        Tr::unpack(ld_coherent_v4(static_cast<const char *>(a.src[d]) + e * S), v);
 #pragma unroll
         for (int i = 0; i < VEC; ++i) {
             held[i] = F::fold(held[i], v[i], a.scale);
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(kCmpThreads) ring_ag_hop_kernel(const __grid_c
         const int c = chunk_of<1>(a, e, 0);
         const char *from = static_cast<const char *>(a.dst[(c + h - 1) % p]) + e * (U / vec_units);
         char *to = static_cast<char *>(a.dst[(c + h) % p]) + e * (U / vec_units);
-        if constexpr (U == 16) st_stream_v4(to, ld_stream_v4(from));
+        if constexpr (U == 16) st_stream_v4(to, ld_coherent_v4(from));
         else if constexpr (U == 4) *reinterpret_cast<uint32_t *>(to) = *reinterpret_cast<const uint32_t *>(from);
         else *reinterpret_cast<uint16_t *>(to) = *reinterpret_cast<const uint16_t *>(from);
     }
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(kCmpThreads) one_phase_kernel(const __grid_con
             uint4 rv[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                if (k0 + j < p) rv[j] = ld_stream_v4(static_cast<const char *>(a.src[a.order[c][k0 + j]]) + e * S);
+                if (k0 + j < p) rv[j] = ld_coherent_v4(static_cast<const char *>(a.src[a.order[c][k0 + j]]) + e * S);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (k0 + j < p) {

@@ -16,10 +16,15 @@
 namespace ccl {
 
 // ---------------------------------------------------------------------------
-// Memory access.  Inputs are streamed once: read through the non-coherent
-// path without allocating in L1, with a 256-byte L2 prefetch hint.  Each
-// element is read and then written by the same thread and by no other, so an
-// in-place operation never reads a value another thread has written.
+// Memory access.  Inputs are streamed once: read without allocating in L1,
+// with a 256-byte L2 prefetch hint.  ld_stream_v4 reads through the
+// non-coherent path, which PTX defines only for data that no thread writes
+// while the kernel runs: it serves launches where no output overlaps an
+// input.  ld_coherent_v4 is the same load without .nc, for in-place launches
+// (an output is an input), where each element is read and then written by
+// the same thread.  Measured on GB300 (AllReduce p=8/16 bf16, p=5/8 fp32, in
+// place and out of place): the two loads run at the same speed within
+// 0.05 %; ReduceScatter p=8 bf16 0.2-0.3 % slower with the coherent load.
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
@@ -29,6 +34,24 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(p));
     return r;
+}
+
+__device__ __forceinline__ uint4 ld_coherent_v4(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p)
+                 : "memory");
+    return r;
+}
+
+// NC: the launch's outputs overlap none of its inputs.
+template <bool NC>
+__device__ __forceinline__ uint4 ld_in_v4(const void *p)
+{
+    if constexpr (NC) return ld_stream_v4(p);
+    else return ld_coherent_v4(p);
 }
 
 __device__ __forceinline__ void st_v4(void *p, const uint4 &v)

@@ -39,6 +39,7 @@ struct Launch {
     const Table *table = nullptr;
     bool vec = false;          // 16-byte vector body allowed
     uint64_t self_mask = 0;    // AllGather: bit r set when dst[r] == src[r] (in place)
+    bool alias = false;        // some output is (part of) an input: in-place loads, no ld.global.nc
     int device = 0;            // the current device while the kernel is launched
     int num_sms = 0;
     int sm_budget = 0;         // 0 = all SMs
@@ -57,6 +58,7 @@ struct LaunchInfo {
     int block = 0;
     size_t smem = 0;
     int kernels = 0;           // kernels launched
+    int counter = 0;           // 1: CTAs or warps took work from a device-wide counter
 };
 
 // TMA variant geometry: tile bytes T per rank per stage and the stage count
@@ -148,11 +150,17 @@ inline bool bulkred_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *
     return false;
 }
 
-// Per-dtype AllReduce / ReduceScatter launchers (ld/st variant).
+// Per-dtype AllReduce / ReduceScatter launchers (ld/st variant).  They pick
+// the in-place instantiation (coherent loads, reduce_{dtype}_inplace.cu)
+// when L.alias is set.
 cudaError_t launch_reduce_f32(const Launch &L, LaunchInfo *info);
 cudaError_t launch_reduce_f16(const Launch &L, LaunchInfo *info);
 cudaError_t launch_reduce_bf16(const Launch &L, LaunchInfo *info);
 cudaError_t launch_reduce_i32(const Launch &L, LaunchInfo *info);
+cudaError_t launch_reduce_inplace_f32(const Launch &L, LaunchInfo *info);
+cudaError_t launch_reduce_inplace_f16(const Launch &L, LaunchInfo *info);
+cudaError_t launch_reduce_inplace_bf16(const Launch &L, LaunchInfo *info);
+cudaError_t launch_reduce_inplace_i32(const Launch &L, LaunchInfo *info);
 
 // Per-dtype AllReduce / ReduceScatter launchers (TMA variant).
 cudaError_t launch_tma_f32(const Launch &L, LaunchInfo *info);

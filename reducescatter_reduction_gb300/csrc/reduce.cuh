@@ -90,7 +90,7 @@ __device__ __forceinline__ void reduce_one(const ReduceArgs<PM> &a, int p, int c
 
 // P > 0: p fixed at compile time (loads fully unrolled); P == 0: any p up to
 // kMaxRanks, loads issued eight at a time.
-template <typename T, int OP, int P, int MODE, bool DYN>
+template <typename T, int OP, int P, int MODE, bool DYN, bool NC>
 __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRanks)> &a)
 {
     using Tr = Traits<T>;
@@ -134,7 +134,7 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
         if constexpr (P > 0) {
             uint4 r[P];
 #pragma unroll
-            for (int k = 0; k < P; ++k) r[k] = ld_stream_v4(sp[k] + e * S);
+            for (int k = 0; k < P; ++k) r[k] = ld_in_v4<NC>(sp[k] + e * S);
             acc.first(r[0], a.scale);
 #pragma unroll
             for (int k = 1; k < P; ++k) acc.fold(r[k], a.scale);
@@ -144,7 +144,7 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     if (k0 + j < p)
-                        r[j] = ld_stream_v4(static_cast<const char *>(a.src[a.order[c][k0 + j]]) + e * S);
+                        r[j] = ld_in_v4<NC>(static_cast<const char *>(a.src[a.order[c][k0 + j]]) + e * S);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     if (k0 + j < p) {
@@ -205,13 +205,13 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
 // 256-thread CTAs per SM).
 // Launched as a dependent: the next kernel may be scheduled once the last
 // wave of CTAs is running.
-template <typename T, int OP, int P, int MODE>
+template <typename T, int OP, int P, int MODE, bool NC>
 __global__ void __launch_bounds__(reduce_threads<P>())
     reduce_kernel(const __grid_constant__ ReduceArgs<(P > 0 ? P : kMaxRanks)> a)
 {
     grid_dependency_wait();
     grid_dependents_launch();
-    reduce_body<T, OP, P, MODE, false>(a);
+    reduce_body<T, OP, P, MODE, false, NC>(a);
 }
 
 // fp32 sum, prod and avg at p = 5 or 6 through the generic kernel: the same
@@ -219,13 +219,13 @@ __global__ void __launch_bounds__(reduce_threads<P>())
 // registers, no spills) instead of its seven.  Measured on GB300 over 4 GiB
 // of inputs, fp32 sum: p=5 6.60 -> 7.15 TB/s, p=6 6.93 -> 7.13.  int32, min
 // and max, and p = 7, gained nothing (within 0.4 % either way).
-template <typename T, int OP, int P, int MODE>
+template <typename T, int OP, int P, int MODE, bool NC>
 __global__ void __launch_bounds__(reduce_threads<P>(), 8)
     reduce_kernel_occ8(const __grid_constant__ ReduceArgs<(P > 0 ? P : kMaxRanks)> a)
 {
     grid_dependency_wait();
     grid_dependents_launch();
-    reduce_body<T, OP, P, MODE, false>(a);
+    reduce_body<T, OP, P, MODE, false, NC>(a);
 }
 
 // fp16/bf16 min/max at p = 8 (the packed select fold): the same body, with
@@ -233,23 +233,23 @@ __global__ void __launch_bounds__(reduce_threads<P>(), 8)
 // of its own four.  The compare -> select chain keeps each thread's loads
 // outstanding for longer than a sum's adds do, so more resident threads pay:
 // 6.72 -> 6.89 TB/s on GB300 (six CTAs: 6.81; at p = 4 neither helped).
-template <typename T, int OP, int P, int MODE>
+template <typename T, int OP, int P, int MODE, bool NC>
 __global__ void __launch_bounds__(reduce_threads<P>(), 5)
     reduce_kernel_occ5(const __grid_constant__ ReduceArgs<(P > 0 ? P : kMaxRanks)> a)
 {
     grid_dependency_wait();
     grid_dependents_launch();
-    reduce_body<T, OP, P, MODE, false>(a);
+    reduce_body<T, OP, P, MODE, false, NC>(a);
 }
 
 // SM budget: one large CTA per SM, so the full register file per thread.
 // Persistent, so the next kernel is scheduled only as its CTAs exit.
-template <typename T, int OP, int P, int MODE>
+template <typename T, int OP, int P, int MODE, bool NC>
 __global__ void __launch_bounds__(reduce_budget_threads<P>(), 1)
     reduce_budget_kernel(const __grid_constant__ ReduceArgs<(P > 0 ? P : kMaxRanks)> a)
 {
     grid_dependency_wait();
-    reduce_body<T, OP, P, MODE, true>(a);
+    reduce_body<T, OP, P, MODE, true, NC>(a);
     if (a.dynamic) {
         __syncthreads();
         if (threadIdx.x == 0 && atomicAdd(a.status + 10, 1u) == gridDim.x - 1) {
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(reduce_budget_threads<P>(), 1)
 // Host side: pick the instantiation, fill the argument block, size the grid.
 // ---------------------------------------------------------------------------
 
-template <typename T, int OP, int P, int MODE>
+template <typename T, int OP, int P, int MODE, bool NC>
 static cudaError_t launch_p(const Launch &L, LaunchInfo *info)
 {
     constexpr int PM = P > 0 ? P : kMaxRanks;
@@ -288,12 +288,12 @@ static cudaError_t launch_p(const Launch &L, LaunchInfo *info)
     const uint64_t units = L.vec ? (L.n / Traits<T>::VEC + L.n % Traits<T>::VEC) : L.n;
     const uint64_t small_grid = (units + reduce_threads<P>() - 1) / reduce_threads<P>();
     const bool budget = L.sm_budget > 0 && L.sm_budget < L.num_sms && small_grid > uint64_t(L.sm_budget);
-    auto kern = budget ? reduce_budget_kernel<T, OP, P, MODE> : reduce_kernel<T, OP, P, MODE>;
+    auto kern = budget ? reduce_budget_kernel<T, OP, P, MODE, NC> : reduce_kernel<T, OP, P, MODE, NC>;
     if constexpr (kSelect16<T, OP> && P == 8) {
-        if (!budget) kern = reduce_kernel_occ5<T, OP, P, MODE>;
+        if (!budget) kern = reduce_kernel_occ5<T, OP, P, MODE, NC>;
     }
     if constexpr (P == 0 && std::is_same<T, F32>::value && OP != OP_MIN && OP != OP_MAX) {
-        if (!budget && L.p <= 6) kern = reduce_kernel_occ8<T, OP, P, MODE>;
+        if (!budget && L.p <= 6) kern = reduce_kernel_occ8<T, OP, P, MODE, NC>;
     }
     const int kThreads = budget ? reduce_budget_threads<P>() : reduce_threads<P>();
     uint64_t want = (units + kThreads - 1) / kThreads;
@@ -325,39 +325,42 @@ static cudaError_t launch_p(const Launch &L, LaunchInfo *info)
         info->block = kThreads;
         info->smem = smem;
         info->kernels = 1;
+        info->counter = a.dynamic;
     }
     return cudaGetLastError();
 }
 
-template <typename T, int OP, int MODE>
+template <typename T, int OP, int MODE, bool NC>
 static cudaError_t launch_op_mode(const Launch &L, LaunchInfo *info)
 {
     switch (L.p) {
-    case 2: return launch_p<T, OP, 2, MODE>(L, info);
-    case 3: return launch_p<T, OP, 3, MODE>(L, info);
-    case 4: return launch_p<T, OP, 4, MODE>(L, info);
-    case 8: return launch_p<T, OP, 8, MODE>(L, info);
-    case 16: return launch_p<T, OP, 16, MODE>(L, info);
-    default: return launch_p<T, OP, 0, MODE>(L, info);
+    case 2: return launch_p<T, OP, 2, MODE, NC>(L, info);
+    case 3: return launch_p<T, OP, 3, MODE, NC>(L, info);
+    case 4: return launch_p<T, OP, 4, MODE, NC>(L, info);
+    case 8: return launch_p<T, OP, 8, MODE, NC>(L, info);
+    case 16: return launch_p<T, OP, 16, MODE, NC>(L, info);
+    default: return launch_p<T, OP, 0, MODE, NC>(L, info);
     }
 }
 
-template <typename T, int OP>
+template <typename T, int OP, bool NC>
 static cudaError_t launch_op(const Launch &L, LaunchInfo *info)
 {
-    return L.mode == MODE_AR ? launch_op_mode<T, OP, MODE_AR>(L, info)
-                             : launch_op_mode<T, OP, MODE_RS>(L, info);
+    return L.mode == MODE_AR ? launch_op_mode<T, OP, MODE_AR, NC>(L, info)
+                             : launch_op_mode<T, OP, MODE_RS, NC>(L, info);
 }
 
-template <typename T>
+// NC = true: no output overlaps an input (ld.global.nc); false: the in-place
+// instantiation, compiled in its own translation unit.
+template <typename T, bool NC>
 static cudaError_t launch_reduce(const Launch &L, LaunchInfo *info)
 {
     switch (L.op) {
-    case OP_SUM: return launch_op<T, OP_SUM>(L, info);
-    case OP_PROD: return launch_op<T, OP_PROD>(L, info);
-    case OP_MIN: return launch_op<T, OP_MIN>(L, info);
-    case OP_MAX: return launch_op<T, OP_MAX>(L, info);
-    case OP_AVG: return launch_op<T, OP_AVG>(L, info);
+    case OP_SUM: return launch_op<T, OP_SUM, NC>(L, info);
+    case OP_PROD: return launch_op<T, OP_PROD, NC>(L, info);
+    case OP_MIN: return launch_op<T, OP_MIN, NC>(L, info);
+    case OP_MAX: return launch_op<T, OP_MAX, NC>(L, info);
+    case OP_AVG: return launch_op<T, OP_AVG, NC>(L, info);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -3,6 +3,9 @@
 
 namespace ccl {
 
-cudaError_t launch_reduce_i32(const Launch &L, LaunchInfo *info) { return launch_reduce<I32>(L, info); }
+cudaError_t launch_reduce_i32(const Launch &L, LaunchInfo *info)
+{
+    return L.alias ? launch_reduce_inplace_i32(L, info) : launch_reduce<I32, true>(L, info);
+}
 
 }  // namespace ccl

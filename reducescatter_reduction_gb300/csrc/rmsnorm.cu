@@ -18,7 +18,9 @@
 // over co-scheduled CTAs: nothing spins.  Each element
 // is read from the rank inputs once; all arithmetic is fp32 with explicit
 // round-to-nearest operations (1/sqrtf is IEEE-rounded under the default
-// flags).  Bytes: (2p + 2) n s + hidden s.
+// flags).  Bytes: (2p + 2) n s + hidden s.  Loads are coherent (no
+// ld.global.nc): the residual is usually updated in place, and the rank
+// outputs may be the inputs.
 #include <cooperative_groups.h>
 
 #include "device.cuh"
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
 #pragma unroll
                     for (int k = 0; k < P; ++k) sp[k] = static_cast<const char *>(a.src[a.order[c][k]]) + e * S;
 #pragma unroll
-                    for (int k = 0; k < P; ++k) r[k] = ld_stream_v4(sp[k]);
+                    for (int k = 0; k < P; ++k) r[k] = ld_coherent_v4(sp[k]);
                     hold_batch(r);
                 } else {
                     // many rows: the compiler's interleaved schedule uses fewer
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
                     // 512-thread CTAs: 193 vs 202 us at 4096 tokens)
 #pragma unroll
                     for (int k = 0; k < P; ++k)
-                        r[k] = ld_stream_v4(static_cast<const char *>(a.src[a.order[c][k]]) + e * S);
+                        r[k] = ld_coherent_v4(static_cast<const char *>(a.src[a.order[c][k]]) + e * S);
                 }
                 Tr::unpack(r[0], acc);
 #pragma unroll
@@ -153,15 +155,15 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
                     for (int i = 0; i < VEC; ++i) acc[i] = F::fold(acc[i], v[i], 1.0f);
                 }
             } else {
-                Tr::unpack(ld_stream_v4(static_cast<const char *>(a.src[a.order[c][0]]) + e * S), acc);
+                Tr::unpack(ld_coherent_v4(static_cast<const char *>(a.src[a.order[c][0]]) + e * S), acc);
                 for (int k = 1; k < p; ++k) {
-                    Tr::unpack(ld_stream_v4(static_cast<const char *>(a.src[a.order[c][k]]) + e * S), v);
+                    Tr::unpack(ld_coherent_v4(static_cast<const char *>(a.src[a.order[c][k]]) + e * S), v);
 #pragma unroll
                     for (int i = 0; i < VEC; ++i) acc[i] = F::fold(acc[i], v[i], 1.0f);
                 }
             }
             Tr::unpack(Tr::pack(acc), acc);                                  // y, rounded
-            Tr::unpack(ld_stream_v4(static_cast<const char *>(a.residual) + e * S), v);
+            Tr::unpack(ld_coherent_v4(static_cast<const char *>(a.residual) + e * S), v);
 #pragma unroll
             for (int i = 0; i < VEC; ++i) acc[i] = __fadd_rn(acc[i], v[i]);   // the merge
             const uint4 hq = Tr::pack(acc);

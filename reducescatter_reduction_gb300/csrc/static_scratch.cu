@@ -1,14 +1,12 @@
 // ccl_allreduce_static: AllReduce for callers that cannot allocate device
 // memory.
 //
-// Who needs it: code that runs where device allocation is off limits or too
-// costly -- a plug-in inside a host application (an inference server, a
-// framework's memory pool) that owns all device memory and forbids further
-// cudaMalloc, a process that has already committed its memory budget, or a
-// latency-critical path where cudaMalloc's implicit device synchronisation and
-// possible failure under memory pressure are not acceptable.  The communicator
-// API allocates a small status block per communicator; this entry point
-// allocates nothing.
+// Who needs it: code that runs where device allocation is off limits -- a
+// plug-in inside a host application (an inference server, a framework's
+// memory pool) that owns all device memory and forbids further cudaMalloc, a
+// process that has already committed its memory budget, or code that must not
+// meet an out-of-memory failure once it runs.  The communicator API allocates
+// a small status block per communicator; this entry point allocates nothing.
 //
 // What it runs: the TMA variant's AllReduce kernel (tma.cuh) with its static
 // tile split (no tile counter).  That kernel's only memory beyond the
@@ -18,6 +16,7 @@
 // every GPU that loads the library holds until the process exits.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -43,6 +42,12 @@ struct DeviceSlot {
 };
 std::mutex g_mu;
 DeviceSlot g_slots[kMaxDevices];
+
+// Test hook (ccl_allreduce_static_set_debug): the bound on each wait of the
+// kernel and the producer's withheld tile.
+constexpr long long kDefaultWaitNs = 2000000000LL;
+std::atomic<long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_stall{0};
 
 ccl_status_t fail(ccl_status_t st, const char *fmt, ...)
 {
@@ -178,8 +183,8 @@ extern "C" ccl_status_t ccl_allreduce_static(int p, void *const *in_ptrs, void *
     L.pipe_bytes = 0;
     L.status = static_cast<unsigned *>(scratch);
     L.tile_counter = false;  // the static split: nothing shared between calls but the status record
-    L.wait_limit_ns = 2000000000LL;
-    L.stall_test = 0;
+    L.wait_limit_ns = g_wait_ns.load();
+    L.stall_test = g_stall.load();
     L.stream = st;
     LaunchInfo info;
     switch (dtype) {
@@ -189,5 +194,15 @@ extern "C" ccl_status_t ccl_allreduce_static(int p, void *const *in_ptrs, void *
     default: err = launch_tma_i32(L, &info); break;
     }
     if (err != cudaSuccess) return cuda_fail(err, "kernel launch");
+    return CCL_OK;
+}
+
+extern "C" ccl_status_t ccl_allreduce_static_set_debug(long long wait_limit_ns, int stall_test)
+{
+    if (wait_limit_ns < 0 || stall_test < 0 || stall_test > 1)
+        return fail(CCL_ERR_INVALID_ARG, "ccl_allreduce_static_set_debug: wait_limit_ns %lld / stall_test %d out of range",
+                    wait_limit_ns, stall_test);
+    g_wait_ns.store(wait_limit_ns ? wait_limit_ns : kDefaultWaitNs);
+    g_stall.store(stall_test);
     return CCL_OK;
 }

@@ -585,6 +585,7 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
         info->block = kTmaThreads;
         info->smem = smem;
         info->kernels = 1;
+        info->counter = a.dynamic;
     }
     return cudaGetLastError();
 }
@@ -636,6 +637,7 @@ static cudaError_t tma_wide_launch(const Launch &L, LaunchInfo *info)
         info->block = kTmaThreads;
         info->smem = smem;
         info->kernels = 1;
+        info->counter = a.dynamic;
     }
     return cudaGetLastError();
 }

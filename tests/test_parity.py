@@ -124,13 +124,24 @@ def test_allreduce_multi_sweep_ragged(p, dtype, op, sched):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_allreduce_in_place(dtype):
-    p, n = 8, (1 << 18) + 5
-    xs = gen(dtype, "sum", p, n, seed=8)
-    res, _ = run_collective(xs, "ar", "sum", dtype, "ring", inplace=True)
-    want = oracle.allreduce(xs, "sum", dtype, "ring")
-    for r in range(p):
-        assert bits_equal(res.host(r), want[r])
+@pytest.mark.parametrize("p,budget", [(8, 0), (8, 2), (5, 0), (16, 2)])
+def test_allreduce_in_place(dtype, p, budget):
+    """In place (outputs are the inputs): the launch takes the instantiation
+    that loads without ld.global.nc (inplace=1); float inputs reveal the
+    accumulation order (inputs.cancel)."""
+    n = p * (1 << 15) + 5
+    if dtype == "i32":
+        xs = gen(dtype, "sum", p, n, seed=8)
+    else:
+        xs = [inputs.cancel(n, 8, r, p, dtype) for r in range(p)]
+    for sched in ("ring", "allpairs"):
+        res, desc = run_collective(xs, "ar", "sum", dtype, sched, inplace=True, budget=budget)
+        assert "inplace=1" in desc and "allreduce_ldst" in desc, desc
+        want = oracle.allreduce(xs, "sum", dtype, sched)
+        for r in range(p):
+            assert bits_equal(res.host(r), want[r])
+    _, desc = run_collective(xs, "ar", "sum", dtype, "ring", budget=budget)
+    assert "inplace=0" in desc, desc
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -172,12 +183,13 @@ def test_reduce_scatter_in_place_nccl_convention(dtype):
     """In place as NCCL defines it: rank r's output is chunk r of its own
     input buffer."""
     p, n = 8, 8 * 40000
-    xs = gen(dtype, "sum", p, n, seed=12)
+    xs = [inputs.cancel(n, 12, r, p, dtype) for r in range(p)]
     storage = inputs.STORAGE[dtype]
     ins = RankBuffers(xs, n, storage)
     with Comm(ins, out_ptrs=[ins.ptr(r, r * (n // p)) for r in range(p)]) as cm:
         ccl.ccl_reduce_scatter(cm.h, "sum", dtype, n, "ring", stream_ptr())
         torch.cuda.synchronize()
+        assert "inplace=1" in ccl.ccl_comm_last_launch(cm.h)
     want = oracle.reduce_scatter(xs, "sum", dtype, "ring")
     for r in range(p):
         got = ins.host(r)[r * (n // p):(r + 1) * (n // p)]
@@ -272,6 +284,34 @@ def test_auto_schedule_follows_cost_model(monkeypatch):
     xs = gen("bf16", "sum", p, 1 << 10, seed=15)
     _, desc = run_collective(xs, "ar", "sum", "bf16", "auto")
     assert "schedule=ring" in desc
+
+
+def test_environment_overrides_apply_only_to_open_choices(monkeypatch):
+    """CCL_SCHEDULE, CCL_VARIANT and CCL_SM_BUDGET change a call only where
+    the call or the communicator left the choice open (schedule auto, variant
+    auto, SM budget 0); values outside their lists are refused, never ignored."""
+    p, n = 8, 8 * (1 << 16)
+    xs = gen("bf16", "sum", p, n, seed=17)
+    want = oracle.allreduce(xs, "sum", "bf16", "allpairs")
+    monkeypatch.setenv("CCL_VARIANT", "tma")
+    monkeypatch.setenv("CCL_SM_BUDGET", "4")
+    monkeypatch.setenv("CCL_SCHEDULE", "allpairs")
+    res, desc = run_collective(xs, "ar", "sum", "bf16", "auto", variant="auto")
+    assert "allreduce_tma" in desc and "sm_budget=4" in desc and "schedule=allpairs" in desc, desc
+    assert bits_equal(res.host(0), want[0])
+    # explicit arguments win
+    res, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="ldst", budget=8)
+    assert "allreduce_ldst" in desc and "sm_budget=8" in desc and "schedule=ring" in desc, desc
+    # AllGather has only the ld/st kernel: the variant override does not apply
+    res, desc = run_collective(xs, "ag", "sum", "bf16", variant="auto")
+    assert "all_gather_ldst" in desc and "sm_budget=4" in desc, desc
+    for var, val in (("CCL_VARIANT", "fast"), ("CCL_SM_BUDGET", "-3"), ("CCL_SM_BUDGET", "4x"),
+                     ("CCL_SCHEDULE", "tree")):
+        monkeypatch.setenv(var, val)
+        with pytest.raises(ccl.CclError) as ei:
+            run_collective(xs, "ar", "sum", "bf16", "auto", variant="auto")
+        assert ei.value.status == ccl.CCL_ERR_INVALID_ARG and var in str(ei.value)
+        monkeypatch.setenv(var, {"CCL_VARIANT": "auto", "CCL_SM_BUDGET": "", "CCL_SCHEDULE": "auto"}[var])
 
 
 def test_side_stream_and_launch_count():

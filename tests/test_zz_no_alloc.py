@@ -2,25 +2,29 @@
 allocate device memory.
 
 Such callers include a plug-in running inside an application that owns all
-device memory (an inference server, a framework's memory pool), a process
-whose memory budget is already committed, and a latency-critical path that
-cannot afford cudaMalloc's implicit synchronisation.  The entry point needs
-no communicator.  It keeps the only scratch its kernel uses, a 16-byte status
-record, in a static device array of the library.
+device memory and hands out only the buffers it manages (an inference
+server, a framework's memory pool), a process whose memory budget is already
+committed, and code that must not meet an out-of-memory failure once it runs.
+The entry point needs no communicator.  It keeps the only scratch its kernel
+uses, a 16-byte status record, in a static device array of the library.
 
-These tests call it through the C ABI and check that two calls in a row give
-exactly the bits of the communicator entry point, ccl_allreduce, on the same
-inputs (bit-exact, as every fixed-order test here). They also check that the
-calls take no device memory. The file sorts last, so a run that stops at the
-first failure has run every other test first.
+These tests call it through the C ABI on inputs whose bits depend on every
+chunk's rank order (inputs.cancel) and check two calls in a row bit for bit
+against the CPU oracle, and against the communicator entry point,
+ccl_allreduce, on the same inputs.  They also check that the calls take no
+device memory, and that a bounded wait that runs out (made to, through the
+test hook) is reported by the next call, which launches nothing, while the
+call after it computes the right bits again.  The file sorts last, so a run
+that stops at the first failure has run every other test first.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import reducescatter_reduction_gb300 as ccl
 from reducescatter_reduction_gb300 import inputs
-from ccl_testutil import Comm, RankBuffers, ensure_built, stream_ptr
+from ccl_testutil import Comm, RankBuffers, bits_equal, ensure_built, stream_ptr
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +43,7 @@ CASES = [  # (dtype, op, schedule, p, n): every chunk a multiple of 16 bytes
 
 
 def _inputs(dtype, p, n, seed):
-    return [inputs.normal(n, seed, r, 1.0, dtype) for r in range(p)]
+    return [inputs.cancel(n, seed, r, p, dtype) for r in range(p)]
 
 
 def _reference(xs, dtype, op, sched):
@@ -60,11 +64,17 @@ def test_static_entry_matches_communicator_entry_on_two_calls():
         xs = _inputs(dtype, p, n, seed=60 + i)
         storage = inputs.STORAGE[dtype]
         bufs.append((xs, RankBuffers(xs, n, storage), RankBuffers(None, n, storage, p=p)))
-    # two calls in a row, no synchronisation in between
+    # two calls in a row; each call waits for the work already queued on the
+    # stream before it launches, so the two kernels run one after the other
     for (dtype, op, sched, p, n), (xs, ins, outs) in zip(CASES, bufs):
         ccl.ccl_allreduce_static(p, ins.ptrs(), outs.ptrs(), op, dtype, n, sched, stream_ptr())
     torch.cuda.synchronize()
     for (dtype, op, sched, p, n), (xs, ins, outs) in zip(CASES, bufs):
+        want = oracle.allreduce(xs, op, dtype, sched)
+        other = oracle.allreduce(xs, op, dtype, "allpairs" if sched == "ring" else "ring")
+        assert not bits_equal(want[0], other[0])     # the inputs reveal the order
+        for r in range(p):
+            assert bits_equal(outs.host(r), want[r]), (dtype, op, r)
         ref = _reference(xs, dtype, op, sched)
         for r in range(p):
             assert torch.equal(outs.views[r], ref.views[r]), (dtype, op, r)
@@ -77,7 +87,7 @@ def test_static_entry_allocates_nothing_and_keeps_working():
     storage = inputs.STORAGE[dtype]
     ins = RankBuffers(xs, n, storage)
     outs = RankBuffers(None, n, storage, p=p)
-    ref = _reference(xs, dtype, op, sched)
+    want = oracle.allreduce(xs, op, dtype, sched)
     ccl.ccl_allreduce_static(p, ins.ptrs(), outs.ptrs(), op, dtype, n, sched, stream_ptr())
     torch.cuda.synchronize()
     free_before, _ = torch.cuda.mem_get_info()
@@ -87,12 +97,43 @@ def test_static_entry_allocates_nothing_and_keeps_working():
     free_after, _ = torch.cuda.mem_get_info()
     assert free_after == free_before          # a device allocation would take at least a 2 MiB page
     for r in range(p):
-        assert torch.equal(outs.views[r], ref.views[r])
+        assert bits_equal(outs.host(r), want[r])
     # in place
     ccl.ccl_allreduce_static(p, ins.ptrs(), ins.ptrs(), op, dtype, n, sched, stream_ptr())
     torch.cuda.synchronize()
     for r in range(p):
-        assert torch.equal(ins.views[r], ref.views[r])
+        assert bits_equal(ins.host(r), want[r])
+
+
+def test_static_entry_reports_a_wait_that_ran_out_on_the_next_call():
+    """The producer withholds its second tile, so a consumer's wait (50 ms
+    here) runs out: the kernel records it in the static array and returns.
+    The next call reports CCL_ERR_TIMEOUT without launching; the one after
+    that runs normally and gives the oracle's bits."""
+    dtype, op, sched, p, n = CASES[0]
+    xs = _inputs(dtype, p, n, seed=72)
+    storage = inputs.STORAGE[dtype]
+    ins = RankBuffers(xs, n, storage)
+    outs = RankBuffers(None, n, storage, p=p)
+    want = oracle.allreduce(xs, op, dtype, sched)
+    try:
+        ccl.ccl_allreduce_static_set_debug(50_000_000, 1)
+        ccl.ccl_allreduce_static(p, ins.ptrs(), outs.ptrs(), op, dtype, n, sched, stream_ptr())
+        torch.cuda.synchronize()                  # the kernel gave up and returned: the context is usable
+    finally:
+        ccl.ccl_allreduce_static_set_debug(0, 0)
+    outs.views[0].zero_()
+    torch.cuda.synchronize()
+    with pytest.raises(ccl.CclError) as ei:
+        ccl.ccl_allreduce_static(p, ins.ptrs(), outs.ptrs(), op, dtype, n, sched, stream_ptr())
+    assert ei.value.status == ccl.CCL_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    assert not bool(outs.views[0].any())          # that call launched nothing
+    ccl.ccl_allreduce_static(p, ins.ptrs(), outs.ptrs(), op, dtype, n, sched, stream_ptr())
+    torch.cuda.synchronize()
+    for r in range(p):
+        assert bits_equal(outs.host(r), want[r])
+    assert outs.guards_intact() and ins.guards_intact()
 
 
 def test_static_entry_rejects_what_it_cannot_take():
@@ -112,3 +153,7 @@ def test_static_entry_rejects_what_it_cannot_take():
     with pytest.raises(ccl.CclError) as ei:
         ccl.ccl_allreduce_static(p, ins.ptrs(), outs.ptrs(), "sum", "bf16", n - 4, "custom", stream_ptr())
     assert ei.value.status == ccl.CCL_ERR_INVALID_ARG
+    for bad in ((-1, 0), (0, 2), (0, -1)):
+        with pytest.raises(ccl.CclError) as ei:
+            ccl.ccl_allreduce_static_set_debug(*bad)
+        assert ei.value.status == ccl.CCL_ERR_INVALID_ARG
