@@ -48,7 +48,9 @@ FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["reducescatter_reduction_gb300/csrc/reduce.cuh",
                   "reducescatter_reduction_gb300/csrc/device.cuh",
                   "reducescatter_reduction_gb300/csrc/reduce_bf16.cu"]
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "allreduce_ldst_p8_bf16_256MiB.md")
+# ncu's DRAM bytes per launch of the headline kernel, with the hash of the
+# kernel source it was taken on (written beside the ncu summary it comes from)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
 
 
 def parse_args(argv=None):
@@ -213,25 +215,23 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    """(DRAM bytes per launch, where they come from): ncu's dram__bytes_read.sum
+    + dram__bytes_write.sum per launch of the headline kernel, as recorded in
+    TRAFFIC_FILE -- only if that capture was taken on the current kernel source
+    (else None, and the reason)."""
+    rel = os.path.relpath(TRAFFIC_FILE, ROOT)
     try:
-        with open(PROFILE_SUMMARY) as f:
-            text = f.read()
-    except OSError:
-        return None
-    src, traffic = None, None
-    for line in text.splitlines():
-        if line.startswith("kernel_source_sha256_16:"):
-            src = line.split(":", 1)[1].strip()
-        if line.startswith("dram_bytes_per_launch:"):
-            try:
-                traffic = float(line.split(":", 1)[1].strip())
-            except ValueError:
-                traffic = None
-    if src != kernel_source_hash():
-        return None
-    return traffic
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        traffic = float(rec["dram_bytes_per_launch"])
+        src = str(rec["kernel_source_sha256_16"])
+    except (OSError, KeyError, ValueError, TypeError):
+        return None, f"no ncu record ({rel} missing or unreadable)"
+    cur = kernel_source_hash()
+    if src != cur:
+        return None, f"{rel} was taken on kernel source {src}; the current source is {cur}: not reported"
+    how = rec.get("how", "")
+    return traffic, f"ncu dram__bytes_read.sum + dram__bytes_write.sum, {rel} (kernel source {src}); {how}".rstrip("; ")
 
 
 # ---------------------------------------------------------------------------
@@ -295,6 +295,7 @@ def run_ours(args, dist: Dist):
     per_launch_ms = local_ms / max(1, launches)
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
     peak, peak_src = hbm_peak()
+    traffic, traffic_src = profiled_traffic() if n == N else (None, "profiling size: no record")
 
     result = {
         "metric": METRIC,
@@ -326,7 +327,8 @@ def run_ours(args, dist: Dist):
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic() if n == N else None,
+            "traffic": traffic,
+            "traffic_source": traffic_src,
             "algorithmic_bytes_per_launch": int(alg_bytes),
             "peak_source": peak_src,
             "kernel": launch_desc.split()[0] if launch_desc else None,

@@ -21,24 +21,28 @@ def test_peak_is_the_measured_copy_bandwidth_else_the_fallback(tmp_path, monkeyp
     assert peak == 6755.8 and src.startswith("measured")
 
 
-def test_traffic_only_while_the_summary_matches_the_kernel_source(tmp_path, monkeypatch):
-    summary = tmp_path / "summary.md"
-    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(summary))
-    assert bench.profiled_traffic() is None                       # no summary
-    summary.write_text("kernel_source_sha256_16: %s\ndram_bytes_per_launch: 4293472938\n"
-                       % bench.kernel_source_hash())
-    assert bench.profiled_traffic() == 4293472938.0
-    summary.write_text("kernel_source_sha256_16: 0000000000000000\ndram_bytes_per_launch: 4293472938\n")
-    assert bench.profiled_traffic() is None                       # taken on another source
+def test_traffic_only_while_the_record_matches_the_kernel_source(tmp_path, monkeypatch):
+    rec = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(rec))
+    traffic, why = bench.profiled_traffic()
+    assert traffic is None and "missing" in why                   # no record
+    rec.write_text(json.dumps({"kernel_source_sha256_16": bench.kernel_source_hash(),
+                               "dram_bytes_per_launch": 4293472938, "how": "scaled from 32 MiB per rank"}))
+    traffic, why = bench.profiled_traffic()
+    assert traffic == 4293472938.0 and "dram__bytes_read.sum" in why and "scaled" in why
+    rec.write_text(json.dumps({"kernel_source_sha256_16": "0000000000000000", "dram_bytes_per_launch": 1}))
+    traffic, why = bench.profiled_traffic()
+    assert traffic is None and "not reported" in why              # taken on another source
 
 
-def test_committed_summary_names_its_source_and_traffic():
-    text = open(bench.PROFILE_SUMMARY).read()
-    lines = {ln.split(":", 1)[0]: ln.split(":", 1)[1].strip() for ln in text.splitlines() if ":" in ln}
-    assert len(lines["kernel_source_sha256_16"]) == 16
-    traffic = float(lines["dram_bytes_per_launch"])
+def test_committed_traffic_record_names_its_source_and_traffic():
+    with open(bench.TRAFFIC_FILE) as f:
+        rec = json.load(f)
+    assert len(rec["kernel_source_sha256_16"]) == 16
+    assert os.path.exists(os.path.join(bench.ROOT, rec["summary"]))
     algorithmic = 2 * bench.P * bench.N * bench.S
-    assert 0.99 < traffic / algorithmic < 1.01
+    assert rec["algorithmic_bytes_per_launch"] == algorithmic
+    assert 0.99 < rec["dram_bytes_per_launch"] / algorithmic < 1.01
 
 
 class _Done:
