@@ -76,6 +76,10 @@ def parse_args(argv=None):
     ap.add_argument("--host-buffers", action="store_true",
                     help="profiling mode: only the zero-copy AllReduce, p=8 bf16 rank buffers of --n elements in "
                          "pinned host memory (inputs and outputs), --sm-budget, warmup + steps calls")
+    ap.add_argument("--collective", choices=["rs", "ag"], default=None,
+                    help="profiling mode: only the p=8 bf16 ReduceScatter (rank r's output = chunk r of a second "
+                         "buffer, as in the rs_ag rows) or the in-place AllGather, --n elements per rank, "
+                         "warmup + steps calls")
     ap.add_argument("--calibrate", action="store_true",
                     help="fit t = alpha + bytes/B per variant and SM budget (p=8 bf16) and print the table")
     ap.add_argument("--n", type=int, default=N,
@@ -593,6 +597,48 @@ def run_rs_ag(args, ins, outs, sptr, stream, peak, n):
     return rows
 
 
+def run_collective_only(args, dist):
+    """Profiling mode: the ReduceScatter or the in-place AllGather of the
+    rs_ag rows alone (same buffers, launch shape and bytes), so that ncu can
+    capture that kernel on a small case."""
+    import torch
+    import __graft_entry__
+    import reducescatter_reduction_gb300 as ccl
+    __graft_entry__.build()
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    n = args.n - args.n % P
+    chunk = n // P
+    ins = [torch.randn(n, device=dev, dtype=torch.float32).to(torch.bfloat16) for _ in range(P)]
+    outs = [torch.empty_like(t) for t in ins]
+    if args.collective == "rs":
+        h = ccl.ccl_comm_create(P, [t.data_ptr() for t in ins])
+        ccl.ccl_comm_set_outputs(h, [outs[r].data_ptr() + r * chunk * S for r in range(P)])
+        call = lambda s: ccl.ccl_reduce_scatter(h, "sum", "bf16", n, "ring", s)
+        nbytes = (P + 1) * n * S
+    else:
+        h = ccl.ccl_comm_create(P, [t.data_ptr() for t in outs])
+        call = lambda s: ccl.ccl_all_gather(h, "bf16", n, s)
+        nbytes = P * n * S
+    s = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        call(s.cuda_stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.steps):
+        call(s.cuda_stream)
+    e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / max(1, args.steps)
+    ccl.ccl_comm_check(h)
+    print(json.dumps({"mode": args.collective, "n_per_rank": n, "us_per_call": round(us, 2),
+                      "GBps": round(nbytes / (us * 1e-6) / 1e9, 1), "algorithmic_bytes": nbytes,
+                      "launch": ccl.ccl_comm_last_launch(h)}), flush=True)
+    ccl.ccl_comm_destroy(h)
+    return 0
+
+
 def calibrate(dev):
     """Per-call device time of the p=8 bf16 AllReduce for the ld/st and TMA
     variants at several SM budgets over 16 KiB .. 256 MiB per rank (CUDA-graph
@@ -1106,6 +1152,8 @@ def main(argv=None):
                           "launch": ccl.ccl_comm_last_launch(h)}), flush=True)
         ccl.ccl_comm_destroy(h)
         return 0
+    if args.collective:
+        return run_collective_only(args, dist)
     if args.calibrate:
         import torch
         import __graft_entry__

@@ -129,10 +129,9 @@ typedef enum {
 } ccl_schedule_t;
 
 typedef enum {
-    CCL_VARIANT_AUTO = 0,    /* the ld/st kernel, measured fastest on GB300 with every SM and under budgets
-                                up to 32 SMs; TMA at p <= 8 on half the SMs or more (not all) from
-                                32 MiB per rank, and at p >= 48 on every SM from 64 MiB per rank, when
-                                the layout allows it */
+    CCL_VARIANT_AUTO = 0,    /* the ld/st or the TMA kernel (the same bits), whichever the measured
+                                launch table estimates faster for the call (see ccl_launch_estimate);
+                                TMA only when the layout allows it */
     CCL_VARIANT_LDST = 1,    /* 128-bit register loads/stores, fixed order */
     CCL_VARIANT_TMA = 2,     /* cp.async.bulk into shared-memory stages, fixed order */
     CCL_VARIANT_TMA_BULKRED = 3, /* cp.reduce.async.bulk: order left to the memory system */
@@ -190,7 +189,8 @@ CCL_API ccl_status_t ccl_comm_set_schedule(ccl_comm_t comm, const uint8_t *order
  *              large CTA per SM.  Larger than the SM count = all SMs.  The
  *              comparison executors and ccl_allreduce_residual_rmsnorm always
  *              use every SM.
- *  variant   : a ccl_variant_t.
+ *  variant   : a ccl_variant_t.  CCL_VARIANT_AUTO consults the launch table
+ *              (ccl_launch_estimate).
  *  pipeline_chunk_bytes : 0 = the variant's default.  For the TMA variants,
  *              the bytes per rank moved per pipeline stage (multiple of 16,
  *              1 KiB .. 32 KiB); a size whose stages do not fit in shared
@@ -369,6 +369,28 @@ CCL_API double ccl_cost_estimate(int p, double nbytes, ccl_schedule_t schedule,
 
 /* The schedule AUTO resolves to: the lower modelled time (ties: ring). */
 CCL_API ccl_schedule_t ccl_select_schedule(int p, double nbytes, const ccl_cost_params_t *params);
+
+/* The measured launch table behind CCL_VARIANT_AUTO (T-CCL, section "Launch
+ * Configuration Tuning": launch configurations profiled offline and ranked
+ * per message size in a table the runtime consults).  The table, compiled
+ * into the library, holds the per-call device time of an AllReduce (sum,
+ * ring) with the ld/st and the TMA kernel at measured points: rank count,
+ * element size, SM budget, bytes per rank (reducescatter_reduction_gb300/
+ * calibrate.py measures it on the GPU it is for).  This call returns, in
+ * *us, the table's estimate for p ranks of `dtype`, `sm_budget` (0 = every
+ * SM; a budget at or above the table's SM count is every SM) and
+ * `bytes_per_rank`, for variant CCL_VARIANT_LDST or CCL_VARIANT_TMA: the
+ * nearest measured rank count and SM budget on a log scale (ties: the
+ * larger), the element size itself, a power law between the two nearest
+ * measured sizes, the smallest size's time below it, and the straight line
+ * through the two largest sizes above it.  AUTO takes TMA exactly when its
+ * estimate is below 0.98 times the ld/st one and the layout allows TMA
+ * (16-byte aligned pointers and chunk boundaries).  No GPU is needed.
+ * Errors: CCL_ERR_INVALID_ARG (NULL us, p outside [1, 64], unknown dtype,
+ * negative budget, another variant), CCL_ERR_UNSUPPORTED (the table has no
+ * point for this element size). */
+CCL_API ccl_status_t ccl_launch_estimate(int p, ccl_dtype_t dtype, int sm_budget, size_t bytes_per_rank, int variant,
+                                         double *us);
 
 /* ---------------------------------------------------------------------------
  * Diagnostics.

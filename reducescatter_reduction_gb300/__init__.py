@@ -44,7 +44,7 @@ EXPORTS = (
     "ccl_comm_create", "ccl_comm_set_outputs", "ccl_comm_set_schedule", "ccl_set_launch", "ccl_comm_set_debug",
     "ccl_comm_destroy", "ccl_comm_check", "ccl_allreduce", "ccl_reduce_scatter", "ccl_all_gather",
     "ccl_allreduce_static", "ccl_allreduce_static_set_debug", "ccl_allreduce_residual_rmsnorm",
-    "ccl_schedule_build", "ccl_schedule_check", "ccl_cost_estimate", "ccl_select_schedule",
+    "ccl_schedule_build", "ccl_schedule_check", "ccl_cost_estimate", "ccl_select_schedule", "ccl_launch_estimate",
     "ccl_last_error", "ccl_comm_last_launch", "ccl_comm_launch_count", "ccl_version",
 )
 
@@ -92,6 +92,7 @@ def load_library(path: str = LIB_PATH):
         "ccl_schedule_check": (i, [i, u64, ctypes.POINTER(u64), ctypes.POINTER(ctypes.c_uint8)]),
         "ccl_cost_estimate": (ctypes.c_double, [i, ctypes.c_double, i, ctypes.POINTER(CostParams)]),
         "ccl_select_schedule": (i, [i, ctypes.c_double, ctypes.POINTER(CostParams)]),
+        "ccl_launch_estimate": (i, [i, i, i, sz, i, ctypes.POINTER(ctypes.c_double)]),
         "ccl_last_error": (ctypes.c_char_p, []),
         "ccl_comm_last_launch": (i, [vp, ctypes.c_char_p, sz]),
         "ccl_comm_launch_count": (u64, [vp]),
@@ -231,6 +232,14 @@ def ccl_cost_estimate(p: int, nbytes: float, schedule, params=None) -> float:
 
 def ccl_select_schedule(p: int, nbytes: float, params=None) -> int:
     return load_library().ccl_select_schedule(int(p), float(nbytes), _params(params))
+
+
+def ccl_launch_estimate(p: int, dtype, sm_budget: int, bytes_per_rank: int, variant) -> float:
+    """The launch table's per-call time estimate (us) for the ld/st or TMA kernel."""
+    us = ctypes.c_double()
+    _check(load_library().ccl_launch_estimate(int(p), _code(DTYPES, dtype), int(sm_budget), int(bytes_per_rank),
+                                              _code(VARIANTS, variant), ctypes.byref(us)))
+    return us.value
 
 
 def ccl_last_error() -> str:

@@ -38,7 +38,7 @@ def _sources():
 
 def _headers():
     return (glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
-            + glob.glob(os.path.join(INCLUDE, "*.h")))
+            + glob.glob(os.path.join(CSRC, "*.inc")) + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def _compile(src: str, extra, verbose: bool) -> str:

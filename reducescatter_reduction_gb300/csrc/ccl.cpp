@@ -194,30 +194,6 @@ extern "C" ccl_schedule_t ccl_select_schedule(int p, double nbytes, const ccl_co
     return (ta >= 0 && ta < tr) ? CCL_SCHED_ALLPAIRS : CCL_SCHED_RING;
 }
 
-// Launch choice (T-CCL, section "Launch Configuration Tuning": measured
-// configurations ranked per message size).  Per-call device time on GB300
-// (bench.py --calibrate, p=8 bf16; bench.py "sm_budgets", p=16 bf16 224 MiB):
-//   every SM:        ld/st at every size (p=8, 256 MiB: 610 vs 661 us for TMA)
-//   8 .. 32 SMs:     ld/st, one large CTA per SM (~102 vs ~75 GB/s per SM)
-//   76 SMs, p=8:     TMA from 64 MiB per rank (164 vs 178 us; 639 vs 712 at
-//                    256 MiB): one register-staged CTA per SM keeps too few
-//                    bytes in flight once half the GPU nears the HBM peak
-//   76 SMs, p=16:    ld/st (6825 vs 5611 GB/s)
-// So AUTO takes the TMA variant only at p <= 8, on at least half of the SMs
-// (but not all), for 32 MiB per rank and more, where its layout allows it.
-static bool auto_prefers_tma(int p, int sm_budget, int num_sms, double bytes_per_rank)
-{
-    const double mib = 1024.0 * 1024.0;
-    // p <= 8 on half the SMs or more (not all): the shared-memory stages hold
-    // more bytes in flight per SM than registers can, from 32 MiB per rank.
-    if (p <= 8 && sm_budget > 0 && sm_budget < num_sms && 2 * sm_budget >= num_sms && bytes_per_rank >= 32.0 * mib)
-        return true;
-    // 48 ranks or more on the whole GPU, from 64 MiB per rank: the wide TMA
-    // kernel edges out the generic ld/st kernel (bf16 p=64 6.95 vs 6.82 TB/s,
-    // p=48 6.92 vs 6.85); at 16 MiB per rank it is 5-8 % behind.
-    return p >= 48 && (sm_budget == 0 || sm_budget >= num_sms) && bytes_per_rank >= 64.0 * mib;
-}
-
 // Environment overrides, as NCCL's NCCL_ALGO / NCCL_PROTO ("Inside NCCL
 // AllReduce", section on the tuner): CCL_SCHEDULE=ring|allpairs|auto,
 // CCL_VARIANT=ldst|tma|tma_bulkred|auto and CCL_SM_BUDGET=<k> apply only where
@@ -482,14 +458,16 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
     if (sm_budget == 0 && !env_sm_budget(&sm_budget))
         return fail(CCL_ERR_INVALID_ARG, "CCL_SM_BUDGET=%s is not a count of SMs", getenv("CCL_SM_BUDGET"));
     // AUTO: CCL_VARIANT if set; else the ld/st kernel, or the TMA variant
-    // where auto_prefers_tma says it is measured faster and the layout allows
-    // it.  AllGather has only the ld/st kernel.
+    // where the measured launch table (launch_table.cpp; T-CCL, "Launch
+    // Configuration Tuning") estimates it faster and the layout allows it.
+    // AllGather has only the ld/st kernel.
     int variant = c->variant;
     if (variant == CCL_VARIANT_AUTO && coll != COLL_AG && !env_variant(&variant))
         return fail(CCL_ERR_INVALID_ARG, "CCL_VARIANT=%s is not ldst, tma, tma_bulkred or auto", getenv("CCL_VARIANT"));
     if (variant == CCL_VARIANT_AUTO) {
         variant = CCL_VARIANT_LDST;
-        if (coll != COLL_AG && n > 0 && auto_prefers_tma(p, sm_budget, c->num_sms, double(n) * double(s))) {
+        if (coll != COLL_AG && n > 0 &&
+            launch_table_prefers_tma(p, int(s), sm_budget, c->num_sms, double(n) * double(s))) {
             uint64_t bounds[kMaxRanks + 1];
             chunk_bounds(p, n, bounds);
             bool ok = true;
@@ -640,7 +618,15 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
              info.kernel, kDtypeName[dtype], coll == COLL_AG ? "copy" : kOpName[op], p, n,
              coll == COLL_AG ? "-" : kSchedName[sched], kVariantName[variant], L.vec ? 1 : 0, info.grid, info.block,
              info.smem, sm_budget, info.counter, alias ? 1 : 0);
-    if (debug_on()) fprintf(stderr, "[ccl] %s\n", c->last);
+    if (debug_on()) {
+        // the launch table's estimate for this call (AllReduce of n*s bytes per rank)
+        double est = -1.0;
+        if ((variant == CCL_VARIANT_LDST || variant == CCL_VARIANT_TMA) && coll == COLL_AR &&
+            !launch_table_estimate(p, int(s), sm_budget, c->num_sms, double(n) * double(s), variant, &est))
+            est = -1.0;
+        if (est >= 0) fprintf(stderr, "[ccl] %s est_time_us=%.2f\n", c->last, est);
+        else fprintf(stderr, "[ccl] %s est_time_us=-\n", c->last);
+    }
     if (err != cudaSuccess) return cuda_fail(err, kCollName[coll]);
     return CCL_OK;
 }

@@ -194,6 +194,14 @@ struct NormLaunch {
 };
 cudaError_t launch_allreduce_rmsnorm(const Launch &L, const NormLaunch &N, LaunchInfo *info);
 
+// The measured launch table (launch_table.cpp): the estimated per-call time
+// (us) of an AllReduce with the ld/st or TMA kernel, and AUTO's choice.
+// num_sms 0 = the SM count of the device the table was measured on.
+bool launch_table_estimate(int p, int elem_bytes, int sm_budget, int num_sms, double bytes_per_rank, int variant,
+                           double *us);
+bool launch_table_prefers_tma(int p, int elem_bytes, int sm_budget, int num_sms, double bytes_per_rank);
+int launch_table_points();
+
 // Sets the message ccl_last_error() returns on this host thread; returns st.
 ccl_status_t record_error(ccl_status_t st, const char *msg);
 

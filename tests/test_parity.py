@@ -591,59 +591,70 @@ def test_dependent_launch_chain(graph):
     assert ins.guards_intact() and b.guards_intact() and c.guards_intact() and d.guards_intact()
 
 
-def test_auto_variant_and_budget_kernels():
-    """AUTO runs the ld/st kernel, except at p <= 8 on at least half of the SMs
-    (not all) for 32 MiB per rank and more, where the TMA variant is measured
-    faster (and at 48 ranks or more, below).  Under a budget a large ld/st message runs one 512/1024-thread CTA
-    per SM; a message that already fits in `budget` small CTAs keeps the
-    regular kernel."""
+def auto_expect(p, dtype, budget, nbytes):
+    """The variant AUTO must take by the launch table's rule (include/ccl.h,
+    ccl_launch_estimate): TMA exactly when its estimate is below 0.98 times
+    the ld/st one (the layouts here all allow TMA)."""
+    try:
+        ldst = ccl.ccl_launch_estimate(p, dtype, budget, nbytes, "ldst")
+        tma = ccl.ccl_launch_estimate(p, dtype, budget, nbytes, "tma")
+    except ccl.CclError:
+        return "ldst"
+    return "tma" if tma < 0.98 * ldst else "ldst"
+
+
+def test_budget_kernel_shapes():
+    """Under a budget a large ld/st message runs one 512/1024-thread CTA per
+    SM; a message that already fits in `budget` small CTAs keeps the regular
+    kernel."""
     p, n = 16, 16 * 65536                                 # 2 MiB per rank: 131072 groups
     xs = gen("bf16", "sum", p, n, seed=52)
-    _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto")
+    _, desc = run_collective(xs, "ar", "sum", "bf16", "ring")
     assert "variant=ldst" in desc and "block=128" in desc
-    _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
+    _, desc = run_collective(xs, "ar", "sum", "bf16", "ring", budget=16)
     assert "variant=ldst" in desc and "grid=16 block=512" in desc
     small = gen("bf16", "sum", p, 16 * 64, seed=54)       # 2 KiB per rank: one 128-thread CTA
-    res, desc = run_collective(small, "ar", "sum", "bf16", "ring", variant="auto", budget=16)
+    res, desc = run_collective(small, "ar", "sum", "bf16", "ring", budget=16)
     assert "variant=ldst" in desc and "grid=1 block=128" in desc
     want = oracle.allreduce(small, "sum", "bf16", "ring")
     assert bits_equal(res.host(3), want[3])
-    half = torch.cuda.get_device_properties(0).multi_processor_count // 2
-    big = gen("bf16", "sum", 8, 1 << 24, seed=55)         # 32 MiB per rank
-    _, desc = run_collective(big, "ar", "sum", "bf16", "ring", variant="auto", budget=half)
-    assert "variant=tma" in desc
-    _, desc = run_collective(big, "ar", "sum", "bf16", "ring", variant="auto", budget=32)
-    assert "variant=ldst" in desc and "block=1024" in desc
-    _, desc = run_collective([x[: 1 << 23] for x in big], "ar", "sum", "bf16", "ring",
-                             variant="auto", budget=half)   # 16 MiB per rank
-    assert "variant=ldst" in desc
 
 
-def test_auto_variant_many_ranks():
-    """At 48 ranks and more on the whole GPU AUTO takes the wide TMA kernel
-    from 64 MiB per rank (measured faster there) and the ld/st kernel below;
-    either way the bits equal the ld/st kernel's."""
-    p = 48
-    grain = 8 * p                      # 16-byte chunk boundaries, as the TMA variant needs
-    ins = [torch.empty(34 << 20, dtype=torch.bfloat16, device="cuda").normal_() for _ in range(p)]
+@pytest.mark.parametrize("p,dtype,budget_frac,rank_bytes", [
+    (8, "bf16", 0.5, 32 << 20), (8, "bf16", 0.5, 16 << 20), (8, "bf16", 0.0, 256 << 20), (8, "bf16", 32, 32 << 20),
+    (2, "f32", 8, 4 << 20), (4, "bf16", 0.5, 64 << 20), (16, "bf16", 0.5, 64 << 20), (48, "bf16", 0.0, 68 << 20),
+    (48, "bf16", 0.0, 8 << 20), (64, "f32", 0.0, 32 << 20), (3, "f32", 16, 1 << 20), (24, "bf16", 76, 16 << 20),
+])
+def test_auto_variant_follows_the_launch_table(p, dtype, budget_frac, rank_bytes):
+    """AUTO takes the kernel the measured launch table estimates faster, and
+    either kernel gives the ld/st kernel's bits.  budget_frac < 1 is a share
+    of the device's SMs (0 = every SM), else an SM count."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    budget = int(budget_frac * sms) if budget_frac < 1 else int(budget_frac)
+    s = inputs.ELEM_BYTES[dtype]
+    grain = p * 16 // s                                   # 16-byte chunk boundaries: TMA may run
+    n = (rank_bytes // s) // grain * grain
+    want_variant = auto_expect(p, dtype, budget, n * s)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    ins = [torch.empty(n, dtype=tdt, device="cuda").normal_() for _ in range(p)]
     outs = [torch.empty_like(t) for t in ins]
     ref = [torch.empty_like(t) for t in ins]
     h = ccl.ccl_comm_create(p, [t.data_ptr() for t in ins])
     try:
-        for n, want in (((34 << 20) // grain * grain, "variant=tma"), ((8 << 20) // grain * grain, "variant=ldst")):
-            ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
-            ccl.ccl_set_launch(h, 0, "auto", 0)
-            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", stream_ptr())
-            desc = ccl.ccl_comm_last_launch(h)
-            ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in ref])
-            ccl.ccl_set_launch(h, 0, "ldst", 0)
-            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", stream_ptr())
-            torch.cuda.synchronize()
-            ccl.ccl_comm_check(h)
-            assert want in desc, desc
-            assert all(torch.equal(a[:n].view(torch.int16), b[:n].view(torch.int16)) for a, b in zip(outs, ref))
+        ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
+        ccl.ccl_set_launch(h, budget, "auto", 0)
+        ccl.ccl_allreduce(h, "sum", dtype, n, "ring", stream_ptr())
+        desc = ccl.ccl_comm_last_launch(h)
+        ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in ref])
+        ccl.ccl_set_launch(h, budget, "ldst", 0)
+        ccl.ccl_allreduce(h, "sum", dtype, n, "ring", stream_ptr())
+        torch.cuda.synchronize()
+        ccl.ccl_comm_check(h)
     finally:
         ccl.ccl_comm_destroy(h)
+    assert f"variant={want_variant}" in desc, desc
+    iv = torch.int16 if s == 2 else torch.int32
+    assert all(torch.equal(a.view(iv), b.view(iv)) for a, b in zip(outs, ref))
 
 
 def test_largest_buffers_64bit_indexing():
