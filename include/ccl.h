@@ -208,8 +208,9 @@ CCL_API ccl_status_t ccl_set_launch(ccl_comm_t comm, int sm_budget, int variant,
  *                  of 2 s.  On expiry the kernel records the wait in the
  *                  status block, stops, and ccl_comm_check() returns
  *                  CCL_ERR_TIMEOUT.
- *  stall_test    : 1 makes the TMA producer withhold its second tile, so that
- *                  the consumers' bounded wait runs out: the timeout path is
+ *  stall_test    : 1 makes the TMA producer withhold its second tile, and the
+ *                  fused RMSNorm's second CTA of a row withhold its partial
+ *                  sum, so that a bounded wait runs out: the timeout path is
  *                  exercised without faulting or hanging the GPU.  0 = off.
  * Errors: CCL_ERR_INVALID_ARG for negative values or stall_test > 1. */
 CCL_API ccl_status_t ccl_comm_set_debug(ccl_comm_t comm, long long wait_limit_ns, int stall_test);
@@ -281,7 +282,11 @@ CCL_API ccl_status_t ccl_all_gather(ccl_comm_t comm, ccl_dtype_t dtype, size_t n
  * output.  Rank buffers follow ccl_allreduce's aliasing rules.  The rounding
  * of y and h is exact; the row's mean square is summed in fp32 in a tree, so
  * out may differ from a fp64 evaluation by one unit in the last place of
- * dtype.  Bytes moved: (2p + 2) n s + hidden s. */
+ * dtype.  Bytes moved: (2p + 2) n s + hidden s.  When a row is spread over a
+ * cluster of CTAs, their exchange of partial sums is a wait bounded by the
+ * communicator's wait limit (ccl_comm_set_debug); one that gives up is
+ * reported by ccl_comm_check() as CCL_ERR_TIMEOUT (that call's outputs are
+ * then wrong; residual_out is complete). */
 CCL_API ccl_status_t ccl_allreduce_residual_rmsnorm(ccl_comm_t comm, ccl_dtype_t dtype, size_t rows, size_t hidden,
                                                     const void *residual_in, void *residual_out, const void *gamma,
                                                     float eps, ccl_schedule_t schedule, void *stream);

@@ -703,6 +703,9 @@ extern "C" ccl_status_t ccl_allreduce_residual_rmsnorm(ccl_comm_t c, ccl_dtype_t
     L.device = c->device;
     L.num_sms = c->num_sms;
     L.stream = static_cast<cudaStream_t>(stream);
+    L.status = c->d_status;
+    L.wait_limit_ns = c->wait_limit_ns;
+    L.stall_test = c->stall_test;
     const int sched = resolve_schedule(c, schedule, double(n) * double(s));
     if (sched < 0)
         return fail(CCL_ERR_INVALID_ARG, "CCL_SCHEDULE=%s is not ring, allpairs or auto", getenv("CCL_SCHEDULE"));

@@ -137,3 +137,38 @@ def test_fused_rmsnorm_statuses():
         assert status("f32", rows, hidden, r.ptr(0), r.ptr(0), outs.ptr(0), 1e-6, "ring", s) == ccl.CCL_ERR_INVALID_ARG
         assert status("f32", 0, hidden, r.ptr(0), r.ptr(0), g.ptr(0), 1e-6, "ring", s) == ccl.CCL_OK
     torch.cuda.synchronize()
+
+
+def test_fused_rmsnorm_exchange_wait_times_out_and_context_survives():
+    """The CTAs of a row exchange their partial sums with a bounded wait.  With
+    the stall hook the second CTA of each row withholds its sum: every wait of
+    the row runs out (50 ms here), is recorded, and the CTAs leave together;
+    ccl_comm_check reports CCL_ERR_TIMEOUT, and the next call, with the hook
+    off, gives the oracle's bits.  Nothing traps or faults."""
+    p, rows, hidden, dtype = 8, 2, 8192, "bf16"   # decode shape: a cluster of CTAs per row
+    n = rows * hidden
+    xs = [inputs.cancel(n, 61, r, p, dtype) for r in range(p)]
+    res = inputs.normal(n, 62, 0, 0.5, dtype)
+    gamma = inputs.normal(hidden, 63, 0, 1.0, dtype)
+    storage = inputs.STORAGE[dtype]
+    ins = RankBuffers(xs, n, storage)
+    outs = RankBuffers(None, n, storage, p=p)
+    r_in = RankBuffers([res], n, storage)
+    r_out = RankBuffers(None, n, storage, p=1)
+    g = RankBuffers([gamma], hidden, storage)
+    with Comm(ins, outs) as cm:
+        ccl.ccl_comm_set_debug(cm.h, 50_000_000, 1)
+        ccl.ccl_allreduce_residual_rmsnorm(cm.h, dtype, rows, hidden, r_in.ptr(0), r_out.ptr(0), g.ptr(0),
+                                           1e-6, "ring", stream_ptr())
+        torch.cuda.synchronize()
+        with pytest.raises(ccl.CclError) as ei:
+            ccl.ccl_comm_check(cm.h)
+        assert ei.value.status == ccl.CCL_ERR_TIMEOUT
+        ccl.ccl_comm_set_debug(cm.h, 0, 0)
+        ccl.ccl_allreduce_residual_rmsnorm(cm.h, dtype, rows, hidden, r_in.ptr(0), r_out.ptr(0), g.ptr(0),
+                                           1e-6, "ring", stream_ptr())
+        torch.cuda.synchronize()
+        ccl.ccl_comm_check(cm.h)
+    check(outs, r_out, xs, res, gamma, rows, hidden, dtype, "ring")
+    for b in (ins, outs, r_in, r_out, g):
+        assert b.guards_intact()
