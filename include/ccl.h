@@ -195,8 +195,16 @@ CCL_API ccl_status_t ccl_comm_set_schedule(ccl_comm_t comm, const uint8_t *order
  *              the bytes per rank moved per pipeline stage (multiple of 16,
  *              1 KiB .. 32 KiB); a size whose stages do not fit in shared
  *              memory for the communicator's p is refused at the collective
- *              call (CCL_ERR_INVALID_ARG).  Results of the fixed-order variants
- *              never depend on it.
+ *              call (CCL_ERR_INVALID_ARG).  The ld/st kernels have no stages
+ *              and ignore it.  Results of the fixed-order variants never
+ *              depend on it.  This is the stage of the shared-memory pipeline
+ *              (T-CCL, "Pipelined Copy and Reduction"), not the multi-MiB
+ *              chunk of a ring pipeline between GPUs ("Inside NCCL
+ *              AllReduce"): with every rank in one GPU's memory there is no
+ *              hop to overlap with the next chunk, and such a chunk would only
+ *              decide which CTA handles which part of the buffer when -- a
+ *              choice the kernels make themselves (a device-wide work counter
+ *              on large messages) and that cannot change any result.
  * Errors: CCL_ERR_INVALID_ARG for a negative budget, an unknown variant or a
  * chunk size outside the range. */
 CCL_API ccl_status_t ccl_set_launch(ccl_comm_t comm, int sm_budget, int variant,

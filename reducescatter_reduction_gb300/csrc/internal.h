@@ -69,6 +69,7 @@ struct LaunchInfo {
 constexpr size_t kTmaSmemLimit = 227 * 1024;
 constexpr int kTmaMaxStages = 8;
 constexpr size_t kTmaCtlBytes = 128;
+constexpr size_t kTmaNarrowCtlBytes = 256;   // narrow kernel: four barrier arrays and a larger control block
 
 inline bool tma_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stages, size_t *smem)
 {
@@ -78,12 +79,12 @@ inline bool tma_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stag
     size_t T = want_tile ? want_tile : (p <= 3 ? 16384 : p <= 8 ? 8192 : p <= 24 ? 4096 : p <= 32 ? 2048 : 1024);
     for (; T >= 1024; T /= 2) {
         const size_t per_stage = size_t(p + 1) * T;
-        size_t S = (kTmaSmemLimit - 2 * kTmaMaxStages * 8 - kTmaCtlBytes) / per_stage;
+        size_t S = (kTmaSmemLimit - 4 * kTmaMaxStages * 8 - kTmaNarrowCtlBytes) / per_stage;
         if (S > size_t(kTmaMaxStages)) S = kTmaMaxStages;
         if (S >= 2) {
             *tile = uint32_t(T);
             *stages = uint32_t(S);
-            *smem = S * per_stage + 2 * S * 8 + kTmaCtlBytes;
+            *smem = S * per_stage + 4 * S * 8 + kTmaNarrowCtlBytes;
             return true;
         }
         if (want_tile) return false;
