@@ -17,8 +17,10 @@
 // the same thread produced (kept in registers, with gamma, for the first few
 // units of each thread) and writes the slice to all p outputs.  The exchange
 // wait is bounded by the communicator's wait limit; on expiry the CTA records
-// it in the status block (ccl_comm_check reports CCL_ERR_TIMEOUT) and the
-// row's CTAs leave together through the hardware cluster barrier.  Each element
+// it in the status block (ccl_comm_check reports CCL_ERR_TIMEOUT), waits once
+// more, bounded, for late writes into its shared memory, and finishes.  The
+// only barrier is the cluster barrier before the first remote write, which
+// every CTA of the row reaches.  Each element
 // is read from the rank inputs once; all arithmetic is fp32 with explicit
 // round-to-nearest operations (1/sqrtf is IEEE-rounded under the default
 // flags).  Bytes: (2p + 2) n s + hidden s.  Loads are coherent (no
@@ -227,8 +229,8 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
     }
     const float part = block_sum(ss, red);
     float total = part;
-    bool gave_up = false;
     if (C > 1) {
+        bool gave_up = false;
         // push: every CTA writes its slice sum into parts[q] of every CTA of the
         // row (itself included) and waits for the C sums to land in its own
         // shared memory -- no cluster barrier round trip, no remote reads.  A
@@ -263,6 +265,19 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
                     gave_up = true;
                     break;
                 }
+            }
+        }
+        if (gave_up) {
+            // A sum is missing (recorded above; this call's outputs are
+            // wrong).  Wait once more, again bounded, so that a late peer's
+            // write is not left to land after this CTA has gone, then go on.
+            uint64_t t1;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+            for (;;) {
+                if (cl_try_wait(lbar, 0)) break;
+                uint64_t t;
+                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+                if (t - t1 > uint64_t(a.wait_ns)) break;
             }
         }
         total = 0.0f;
@@ -304,7 +319,6 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
             for (int k = 0; k < p; ++k) Tr::store1(a.dst[k], e, o);
         }
     }
-    if (__syncthreads_or(gave_up)) cluster.sync();   // a wait gave up: leave only together
 }
 
 template <typename T, int P>

@@ -142,7 +142,8 @@ def test_fused_rmsnorm_statuses():
 def test_fused_rmsnorm_exchange_wait_times_out_and_context_survives():
     """The CTAs of a row exchange their partial sums with a bounded wait.  With
     the stall hook the second CTA of each row withholds its sum: every wait of
-    the row runs out (50 ms here), is recorded, and the CTAs leave together;
+    the row runs out (50 ms here), is recorded, and the CTAs finish after a
+    second bounded wait;
     ccl_comm_check reports CCL_ERR_TIMEOUT, and the next call, with the hook
     off, gives the oracle's bits.  Nothing traps or faults."""
     p, rows, hidden, dtype = 8, 2, 8192, "bf16"   # decode shape: a cluster of CTAs per row
