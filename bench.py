@@ -358,6 +358,8 @@ def run_ours(args, dist: Dist):
     if not args.no_budgets:
         torch.cuda.empty_cache()
         result["sm_budgets"] = run_budgets(dev, sptr, stream, peak)
+        result["sm_budgets_p8"] = run_budgets(dev, sptr, stream, peak, p=8, n=1 << 25, variants=("ldst", "tma", "auto"),
+                                              budgets=(8, 16, 32, 76, 0))
         result["fused_rmsnorm"] = run_rmsnorm(dev, peak)
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline_from(ins)
@@ -773,14 +775,15 @@ def run_rmsnorm(dev, peak):
     return rows_out
 
 
-def run_budgets(dev, sptr, stream, peak):
-    """MoE hidden-state AllReduce, p=16 bf16 [16384, 7168] per rank (224 MiB,
-    3.5 GiB in + 3.5 GiB out), ring, at SM budgets from 4 SMs to the whole GPU,
-    ld/st and TMA variants (T-CCL's restricted-CTA-budget comparison)."""
+def run_budgets(dev, sptr, stream, peak, p=16, n=16384 * 7168, variants=("ldst", "tma", "tma_bulkred"),
+                budgets=(4, 8, 16, 32, 76, 0)):
+    """At SM budgets from 4 SMs to the whole GPU, per variant (T-CCL's
+    restricted-CTA-budget comparison).  Default: the MoE hidden-state
+    AllReduce, p=16 bf16 [16384, 7168] per rank (224 MiB, 3.5 GiB in +
+    3.5 GiB out), ring; also run at p=8, 32 MiB per rank."""
     import torch
     import reducescatter_reduction_gb300 as ccl
 
-    p, n = 16, 16384 * 7168
     nbytes = 2 * p * n * S
     ins = [torch.randn(n, device=dev, dtype=torch.float32).to(torch.bfloat16) for _ in range(p)]
     outs = [torch.empty_like(t) for t in ins]
@@ -788,8 +791,8 @@ def run_budgets(dev, sptr, stream, peak):
     ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     rows = []
-    for variant in ("ldst", "tma", "tma_bulkred"):
-        for budget in (4, 8, 16, 32, 76, 0):
+    for variant in variants:
+        for budget in budgets:
             ccl.ccl_set_launch(h, budget, variant, 0)
             for _ in range(2):
                 ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", sptr)
