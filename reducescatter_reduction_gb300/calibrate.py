@@ -79,7 +79,7 @@ def _time_us(call, torch, stream):
     return best
 
 
-def measure(quick=False, log=print):
+def measure(quick=False, log=print, p_points=None, budgets=None, sizes=None):
     import torch
     import reducescatter_reduction_gb300 as ccl
     from reducescatter_reduction_gb300 import build
@@ -89,12 +89,13 @@ def measure(quick=False, log=print):
     dev = torch.device("cuda", torch.cuda.current_device())
     props = torch.cuda.get_device_properties(dev)
     stream = torch.cuda.Stream(dev)
-    p_points = [2, 8, 16, 64] if quick else P_POINTS
-    budgets = [8, 76, 0] if quick else BUDGETS
+    p_points = p_points or ([2, 8, 16, 64] if quick else P_POINTS)
+    budgets = budgets or ([8, 76, 0] if quick else BUDGETS)
+    sizes = sizes or SIZES
     rows = []
     with torch.cuda.stream(stream):
         for p in p_points:
-            max_rank_bytes = min(SIZES[-1], MAX_INPUT_BYTES // p)
+            max_rank_bytes = min(sizes[-1], MAX_INPUT_BYTES // p)
             ins = [torch.empty(max_rank_bytes, dtype=torch.uint8, device=dev).random_() for _ in range(p)]
             outs = [torch.empty(max_rank_bytes, dtype=torch.uint8, device=dev) for _ in range(p)]
             comm = ccl.ccl_comm_create(p, [t.data_ptr() for t in ins])
@@ -103,7 +104,7 @@ def measure(quick=False, log=print):
                 for es, dtype in ELEM_BYTES.items():
                     for budget in budgets:
                         stopped = {"ldst": False, "tma": False}
-                        for nbytes in SIZES:
+                        for nbytes in sizes:
                             if nbytes > max_rank_bytes:
                                 break
                             n = nbytes // es

@@ -117,3 +117,20 @@ def test_render_round_trips():
     assert got[0] == ("2", "4", "8", str(1 << 20), "12.500", "13.250")        # sorted by p first
     assert got[1] == ("8", "2", "0", "16384", "2.150", "3.600")
     assert got[-1] == ("0", "0", "0", "0", "0.0", "0.0")                      # the end marker
+
+
+@pytest.mark.gpu
+def test_calibration_script_measures_and_renders_a_table():
+    """The script that writes the launch table runs on the GPU (a reduced grid)
+    and its rendering parses back into the rows it measured."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    table = calibrate.measure(p_points=[2, 8], budgets=[8, 0], sizes=[16 << 10, 1 << 20], log=lambda s: None)
+    rows = table["rows"]
+    assert {(r["p"], r["elem_bytes"], r["sm_budget"]) for r in rows} == {
+        (p, es, b) for p in (2, 8) for es in (2, 4) for b in (8, 0)}
+    assert all(r["us_ldst"] > 0 and r["us_tma"] > 0 for r in rows)
+    assert table["sms"] == torch.cuda.get_device_properties(0).multi_processor_count
+    parsed = [m.groups() for m in ROW.finditer(calibrate.render(table))]
+    assert len(parsed) == len(rows) + 1                                    # rows and the end marker
