@@ -191,18 +191,21 @@ def test_tma_statuses():
     torch.cuda.synchronize()
 
 
-def test_tma_bounded_wait_times_out_and_context_survives():
+@pytest.mark.parametrize("p,budget,tile", [(8, 1, 4096), (16, 1, 4096), (8, 0, 0), (5, 3, 0), (16, 0, 0)])
+def test_tma_bounded_wait_times_out_and_context_survives(p, budget, tile):
     """The producer withholds a tile (a wait nothing will satisfy); the
     consumers' wait gives up after 20 ms, the kernel records it and returns,
     ccl_comm_check reports CCL_ERR_TIMEOUT once, and the same communicator
-    then runs correctly."""
-    p, n = 8, 8 * (1 << 16)
+    then runs correctly.  p = 5 and 8 run the kernel whose consumer warps wait
+    on the stage barriers themselves (with its store warp), p = 16 the form
+    with the consumer barrier; one CTA or many."""
+    n = p * (1 << 16)
     xs = gen("bf16", "sum", p, n, seed=45)
     storage = inputs.STORAGE["bf16"]
     ins = RankBuffers(xs, n, storage)
     outs = RankBuffers(None, n, storage, p=p)
     with Comm(ins, outs) as cm:
-        ccl.ccl_set_launch(cm.h, 1, "tma", 4096)                 # one CTA walks every tile
+        ccl.ccl_set_launch(cm.h, budget, "tma", tile)
         ccl.ccl_comm_set_debug(cm.h, 20_000_000, 1)
         ccl.ccl_allreduce(cm.h, "sum", "bf16", n, "ring", stream_ptr())
         with pytest.raises(ccl.CclError) as ei:
