@@ -64,19 +64,40 @@ struct LaunchInfo {
 // TMA variant geometry: tile bytes T per rank per stage and the stage count
 // S for p ranks.  A stage holds p input tiles and one output tile; S fills
 // the 227 KB of shared memory one CTA may address (one CTA per SM).  T-CCL
-// ("Experimental Environment") uses 8 KB chunks; T shrinks with p so that at
-// least two stages fit.  want_tile != 0 forces T.  False if no geometry fits.
+// ("Experimental Environment") uses 8 KB chunks.  want_tile != 0 forces T.
+// False if no geometry fits.
 constexpr size_t kTmaSmemLimit = 227 * 1024;
 constexpr int kTmaMaxStages = 8;
 constexpr size_t kTmaCtlBytes = 128;
-constexpr size_t kTmaNarrowCtlBytes = 256;   // narrow kernel: four barrier arrays and a larger control block
+constexpr size_t kTmaNarrowCtlBytes = 256;   // pipelined kernels: four barrier arrays and a larger control block
 
-inline bool tma_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stages, size_t *smem)
+// Grids of at most this many CTAs (an SM budget) take larger narrow tiles.
+constexpr int kTmaSmallGrid = 32;
+
+// Default narrow tile.  Each bulk copy costs the SM's copy engine a fixed
+// time (about 50 ns, measured on GB300: under a budget p=8 moves 35 / 65 /
+// 90 / 103 GB/s per SM with 2 / 4 / 6 / 8 KB tiles), so on a few SMs the
+// largest tile that leaves two stages wins; across many SMs more, smaller
+// stages hide DRAM latency better.  Measured (AllReduce, bf16, GB/s per SM at
+// 8-32 SMs; whole-GPU GB/s):
+//   p=2, 3: 16 KB (whole GPU p=2: 7112 vs 6712 with 8 KB; p=3: 7070 vs 6413)
+//   p=4: 16 KB on small grids (95 vs 82 per SM), 8 KB otherwise (76 SMs: 80 vs 75)
+//   p=5: 12 KB (101 vs 80; 76 SMs 85 vs 77; whole GPU within 0.4 %)
+//   p=6: 12 KB on small grids (90 vs 82), 8 KB otherwise (76 SMs: 81 vs 72)
+//   p=7 .. 13: 8 KB (p=12: 99 vs 67 with 4 KB; p=7 with 12 KB: +3 % on 8 SMs, -10 % on 76)
+inline size_t tma_default_tile(int p, int sm_budget)
 {
-    // measured on GB300 (bf16, all SMs): 16 KB at p <= 3 (p=2: 7112 vs 6712
-    // GB/s with 8 KB; p=3: 7070 vs 6413); 4 KB up to p = 24, where two stages
-    // of 4 KB still fit (p=20: 7000 vs 6234 with 2 KB; p=24: 6993 vs 6622)
-    size_t T = want_tile ? want_tile : (p <= 3 ? 16384 : p <= 8 ? 8192 : p <= 24 ? 4096 : p <= 32 ? 2048 : 1024);
+    const bool small = sm_budget > 0 && sm_budget <= kTmaSmallGrid;
+    if (p <= 3) return 16384;
+    if (p == 4) return small ? 16384 : 8192;
+    if (p == 5) return 12288;
+    if (p == 6) return small ? 12288 : 8192;
+    return 8192;
+}
+
+inline bool tma_geometry(int p, size_t want_tile, int sm_budget, uint32_t *tile, uint32_t *stages, size_t *smem)
+{
+    size_t T = want_tile ? want_tile : tma_default_tile(p, sm_budget);
     for (; T >= 1024; T /= 2) {
         const size_t per_stage = size_t(p + 1) * T;
         size_t S = (kTmaSmemLimit - 4 * kTmaMaxStages * 8 - kTmaNarrowCtlBytes) / per_stage;
@@ -93,13 +114,19 @@ inline bool tma_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *stag
 }
 
 // Above kTmaNarrowMaxRanks ranks a stage holding one tile of every rank
-// would force 1 KB tiles (p+1 of them per stage), and 1 KB bulk copies cost
-// more per byte.  The wide geometry keeps T bytes per copy and brings the p
-// ranks through the stages R at a time (a tile takes ceil(p/R) stages); two
-// output tiles sit beside the stages.  T <= 8 KB so that each consumer
-// thread folds at most two 16-byte groups per tile in registers.
-constexpr int kTmaNarrowMaxRanks = 32;
+// would force tiles below 8 KB (p+1 of them per stage, two stages), and
+// smaller bulk copies cost more per byte.  The wide geometry keeps 8 KB per
+// copy and brings the p ranks through the stages R at a time (a tile takes
+// ceil(p/R) stages); kTmaWideOut output tiles sit beside the stages.  T <=
+// 8 KB so that each consumer thread folds at most two 16-byte groups per tile
+// in registers.  Measured on GB300 (AllReduce, bf16), wide against narrow:
+// p=14 on 16 SMs 84 vs 84 GB/s per SM (6 KB tiles), on 76 SMs 81 vs 77, whole
+// GPU +1 %; p=16 90 vs 78 (4 KB tiles); p=24 93 vs 77; p=32 93 vs 48 (2 KB);
+// p=13 83 vs 99 (narrow, 8 KB tiles) -- so the wide kernel from 14 ranks.
+// More output tiles (3 or 4) measured the same as two.
+constexpr int kTmaNarrowMaxRanks = 13;
 constexpr int kTmaWideRanks = 8;          // R: ranks per stage
+constexpr int kTmaWideOut = 2;            // output tiles
 
 inline bool tma_wide_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *ranks, uint32_t *stages,
                               size_t *smem)
@@ -107,14 +134,15 @@ inline bool tma_wide_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t 
     const size_t T = want_tile ? want_tile : 8192;
     if (T > 8192 || T < 1024) return false;
     const size_t R = size_t(p) < size_t(kTmaWideRanks) ? size_t(p) : size_t(kTmaWideRanks);
-    const size_t fixed = 2 * T + 2 * kTmaMaxStages * 8 + kTmaCtlBytes;
+    // out tiles, four barrier arrays (full/empty per stage, folded/out_free per out tile), control block
+    const size_t fixed = kTmaWideOut * T + 2 * (kTmaMaxStages + kTmaWideOut) * 8 + kTmaNarrowCtlBytes;
     size_t S = (kTmaSmemLimit - fixed) / (R * T);
     if (S > size_t(kTmaMaxStages)) S = kTmaMaxStages;
     if (S < 2) return false;
     *tile = uint32_t(T);
     *ranks = uint32_t(R);
     *stages = uint32_t(S);
-    *smem = S * R * T + 2 * T + 2 * S * 8 + kTmaCtlBytes;
+    *smem = S * R * T + kTmaWideOut * T + 2 * (S + kTmaWideOut) * 8 + kTmaNarrowCtlBytes;
     return true;
 }
 

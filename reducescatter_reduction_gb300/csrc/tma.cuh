@@ -28,9 +28,9 @@
 // mbarrier.  Measured on GB300 against one thread per CTA waiting and
 // issuing behind a 256-thread named barrier (AllReduce, GB/s per SM):
 // p=8 on 8/16/32 SMs 97 -> 105/104/103, p=4 on 16 SMs 70 -> 82, p=5 fp32
-// +27-30 %, p=3 +11 %, p=2 +5-8 %, the whole GPU unchanged -- but p=16 on
-// 16 SMs 78 -> 73, so the p=16 instantiation keeps the barrier form
-// (tma_reduce_sync_kernel below).
+// +27-30 %, p=3 +11 %, p=2 +5-8 %, the whole GPU unchanged; the wide kernel
+// in the same form against its barrier form: p=40 and 64 on 8-32 SMs 70 ->
+// 93, on 76 SMs +25 %.
 //
 // Order, rounding and therefore every bit equal the ld/st kernel's.  Every
 // wait is bounded by %globaltimer: on expiry the kernel records where it gave
@@ -41,9 +41,9 @@
 // boundary and pointer is 16-byte aligned).  The counter lives in the
 // communicator's status block and the last CTA of a launch returns it to
 // zero, so launches on one status block must be ordered (one stream, or
-// synchronised), as every collective on one communicator already is.  Above
-// 32 ranks the wide kernel further down takes over (ranks through the stages
-// eight at a time).
+// synchronised), as every collective on one communicator already is.  From
+// 14 ranks the wide kernel further down takes over (ranks through the stages
+// eight at a time, 8 KB per copy).
 #pragma once
 
 #include "device.cuh"
@@ -52,7 +52,6 @@ namespace ccl {
 
 constexpr int kTmaConsumerWarps = 8;
 constexpr int kTmaConsumers = 32 * kTmaConsumerWarps;
-constexpr int kTmaThreads = kTmaConsumers + 32;
 
 template <int PM>
 struct TmaArgs {
@@ -151,11 +150,6 @@ __device__ __forceinline__ void bulk_wait_read(uint32_t pending)
 
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void consumer_barrier()
-{
-    asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers) : "memory");
-}
-
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr)
 {
     uint4 v;
@@ -215,166 +209,6 @@ __device__ __forceinline__ bool bounded_wait(const TmaArgs<PM> &a, volatile Ctl 
     }
     return true;
 }
-
-// The barrier form: consumer thread 0 waits for each stage and issues its
-// stores behind a 256-thread named barrier.  Kept for p = 16, where it
-// measured 5 % faster than tma_reduce_kernel under SM budgets.
-template <typename T, int OP, int P, int MODE>
-__global__ void __launch_bounds__(kTmaThreads, 1)
-    tma_reduce_sync_kernel(const __grid_constant__ TmaArgs<(P > 0 ? P : kMaxRanks)> a)
-{
-    using Tr = Traits<T>;
-    constexpr int VEC = Tr::VEC;
-    constexpr int S_ELEM = (VEC == 8) ? 2 : 4;
-    extern __shared__ __align__(128) unsigned char smem[];
-
-    const int p = P > 0 ? P : a.p;
-    const uint32_t TB = a.tile_bytes, S = a.stages;
-    unsigned char *in_base = smem;                                   // [S][p][TB]
-    unsigned char *out_base = smem + size_t(S) * p * TB;             // [S][TB]
-    uint64_t *full = reinterpret_cast<uint64_t *>(out_base + size_t(S) * TB);
-    uint64_t *empty = full + S;
-    volatile TmaCtl *ctl = reinterpret_cast<volatile TmaCtl *>(empty + S);
-
-    if (threadIdx.x == 0) {
-        for (uint32_t s = 0; s < S; ++s) {
-            mbar_init(smem_addr(&full[s]), 1);
-            mbar_init(smem_addr(&empty[s]), kTmaConsumerWarps);
-        }
-        ctl->abort = 0;
-        ctl->go = 0;
-        ctl->issued = 0;
-        ctl->consumed = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        fence_proxy_async_smem();
-    }
-    __syncthreads();
-    // Launched as a dependent: the set-up above overlaps the previous
-    // kernel's tail; no global memory is touched before this wait.
-    grid_dependency_wait();
-
-    const uint64_t ntiles = a.tstart[p];
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-    if (warp == 0) {
-        // ------------------------------ producer ------------------------------
-        if (lane == 0) {
-            // Large messages (a.dynamic): tiles go out kTmaGrab at a time,
-            // each CTA's first grab statically (tiles blockIdx.x*G ...), the
-            // rest from a device-wide counter (the status block's words 4-5),
-            // so SMs that run faster take more.  Small messages: tile b, then
-            // b + gridDim.x, ... with no counter, which keeps their latency.
-            unsigned long long *next = reinterpret_cast<unsigned long long *>(a.status + 4);
-            const unsigned long long G = a.dynamic ? kTmaGrab : 1;
-            int c = 0;
-            unsigned long long t = blockIdx.x * G, left = G;   // the current grab: tiles t, t+1, ...
-            for (uint32_t i = 0;; ++i) {
-                const uint32_t s = i % S;
-                if (i >= S && !bounded_wait(a, ctl, smem_addr(&empty[s]), ((i / S) - 1) & 1u, 2u, i)) break;
-                if (a.stall_test && i == 1) break;  // withhold this stage: its consumers must time out
-                if (left == 0) {
-                    t = a.dynamic ? gridDim.x * G + atomicAdd(next, G) : t + gridDim.x;
-                    left = G;
-                } else if (i > 0) {
-                    ++t;
-                }
-                --left;
-                const uint32_t bar = smem_addr(&full[s]);
-                if (t >= ntiles) {
-                    ctl->tile_of[s] = kNoTile;
-                    mbar_arrive(bar);                // no bytes: the consumers wake and stop
-                    break;
-                }
-                ctl->tile_of[s] = t;
-                while (t >= a.tstart[c + 1]) ++c;
-                const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
-                const uint64_t off = cb + (t - a.tstart[c]) * TB;
-                const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
-                mbar_arrive_expect_tx(bar, uint32_t(p) * bytes);
-                unsigned char *slot = in_base + size_t(s) * p * TB;
-                for (int k = 0; k < p; ++k)
-                    bulk_load(smem_addr(slot + size_t(k) * TB),
-                              static_cast<const char *>(a.src[a.order[c][k]]) + off, bytes, bar);
-                ctl->issued = i + 1;
-            }
-        }
-    } else {
-        // ------------------------------ consumers -----------------------------
-        const int tid = threadIdx.x - 32;
-        int c = 0;
-        uint32_t i = 0;
-        for (;; ++i) {
-            const uint32_t s = i % S;
-            if (tid == 0) {
-                bool ok = bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, i);
-                if (ok && i >= S) bulk_wait_read(S - 1);  // out tile s: its stores from tile i-S read it
-                ctl->go = ok ? 1 : 0;
-            }
-            consumer_barrier();
-            if (!ctl->go) break;
-            const unsigned long long t = ctl->tile_of[s];
-            if (t == kNoTile) break;
-            while (t >= a.tstart[c + 1]) ++c;
-            const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
-            const uint64_t off = cb + (t - a.tstart[c]) * TB;
-            const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
-            const uint32_t in_s = smem_addr(in_base + size_t(s) * p * TB);
-            const uint32_t out_s = smem_addr(out_base + size_t(s) * TB);
-            for (uint32_t g = tid; g < bytes / 16; g += kTmaConsumers) {
-                GroupFold<T, OP> acc;
-                if constexpr (P > 0) {
-                    uint4 r[P];
-#pragma unroll
-                    for (int k = 0; k < P; ++k) r[k] = lds_v4(in_s + k * TB + g * 16);
-                    acc.first(r[0], a.scale);
-#pragma unroll
-                    for (int k = 1; k < P; ++k) acc.fold(r[k], a.scale);
-                } else {
-                    acc.first(lds_v4(in_s + g * 16), a.scale);
-                    for (int k = 1; k < p; ++k) acc.fold(lds_v4(in_s + k * TB + g * 16), a.scale);
-                }
-                sts_v4(out_s + g * 16, acc.finish(p));
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&empty[s]));  // input slots of stage s are free
-            fence_proxy_async_smem();                          // out tile visible to the bulk stores
-            consumer_barrier();
-            if (tid == 0) {
-                if constexpr (MODE == MODE_AR) {
-                    for (int k = 0; k < p; ++k) bulk_store(static_cast<char *>(a.dst[k]) + off, out_s, bytes);
-                } else {
-                    bulk_store(static_cast<char *>(a.dst[c]) + (off - cb), out_s, bytes);
-                }
-                bulk_commit();
-                ctl->consumed = i + 1;
-            }
-        }
-        if (tid == 0) bulk_wait_all();
-    }
-    __syncthreads();
-    // After an abort, wait (bounded) for loads still in flight into shared
-    // memory before the CTA gives its shared memory back.
-    if (threadIdx.x == 0 && ctl->abort) {
-        const uint32_t issued = ctl->issued;
-        for (uint32_t j = ctl->consumed; j < issued; ++j) {
-            const uint32_t bar = smem_addr(&full[j % S]);
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(bar, (j / S) & 1u))
-                if (global_ns() - t0 > uint64_t(a.wait_ns)) break;
-        }
-    }
-    // The last CTA to finish takes no more tiles than any other; it returns
-    // the tile counter to zero for the next launch on this status block.
-    // (Each CTA's last counter read has returned before it counts itself
-    // done, so the reset follows every read of this launch.)
-    if (a.dynamic && threadIdx.x == 0) {
-        if (atomicAdd(a.status + 6, 1u) == gridDim.x - 1) {
-            atomicExch(reinterpret_cast<unsigned long long *>(a.status + 4), 0ull);
-            atomicExch(a.status + 6, 0u);
-        }
-    }
-}
-
 
 constexpr int kTmaPipeThreads = kTmaConsumers + 64;   // producer warp, store warp, 8 consumer warps
 
@@ -497,6 +331,13 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
             const uint32_t s = i % S;
             if (!__all_sync(0xffffffffu, bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, i))) break;
             const unsigned long long t = ctl->tile_of[s];
+            // Out tile s must be free before this warp touches it or its
+            // barrier -- also on the last visit: until the store warp has
+            // read out_of[s] of tile i-S, a fast warp must neither overwrite
+            // it nor arrive on folded[s] within that tile's phase.
+            if (i >= S &&
+                !__all_sync(0xffffffffu, bounded_wait(a, ctl, smem_addr(&out_free[s]), ((i / S) - 1) & 1u, 4u, i)))
+                break;
             if (t == kNoTile) {
                 // no more work: tell the store warp through the out tile's barrier
                 if (cw == 0 && lane == 0) ctl->out_of[s] = kNoTile;
@@ -504,9 +345,6 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
                 if (lane == 0) mbar_arrive(smem_addr(&folded[s]));
                 break;
             }
-            if (i >= S &&
-                !__all_sync(0xffffffffu, bounded_wait(a, ctl, smem_addr(&out_free[s]), ((i / S) - 1) & 1u, 4u, i)))
-                break;
             while (t >= a.tstart[c + 1]) ++c;
             const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
             const uint64_t off = cb + (t - a.tstart[c]) * TB;
@@ -561,46 +399,54 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Wide variant (p > kTmaNarrowMaxRanks): a tile's p ranks pass through the
-// stages R at a time.  The producer loads ranks order[c][b*R ...] of tile t
-// into a stage (one stage per batch b = 0 .. B-1, B = ceil(p/R)); each
-// consumer thread keeps the fp32 partial of its 16-byte groups of the tile
-// in registers across the B batches, folding in the chunk's order exactly as
-// the narrow kernel does, and after the last batch writes the tile to one of
-// two output tiles, from which one thread issues the bulk fan-out stores.
-// Waits, abort, drain and the tile counter work as in the narrow kernel (one
-// tile per visit: a tile is B stages of work).
+// Wide variant: a tile's p ranks pass through the stages R at a time.  The
+// producer loads ranks order[c][b*R ...] of tile t into a stage (one stage
+// per batch b = 0 .. B-1, B = ceil(p/R)); each consumer thread keeps the fp32
+// partial of its 16-byte groups of the tile in registers across the B
+// batches, folding in the chunk's order exactly as the narrow kernel does,
+// and after the last batch writes the tile to one of kTmaWideOut output
+// tiles, from which the store warp issues the bulk fan-out stores.  The roles
+// and their mbarriers are the narrow kernel's (producer warp, store warp,
+// 8 consumer warps each waiting for itself), except that the output tiles
+// are not tied to the stages: out tile k % kTmaWideOut holds the CTA's k-th
+// finished tile.  Waits, abort, drain and the tile counter work as in the
+// narrow kernel (one tile per visit: a tile is B stages of work).
 // ---------------------------------------------------------------------------
 
 constexpr int kTmaWideGroups = 2;  // 16-byte groups per consumer thread per tile (T <= 8 KB)
 
 template <typename T, int OP, int MODE>
-__global__ void __launch_bounds__(kTmaThreads, 1)
+__global__ void __launch_bounds__(kTmaPipeThreads, 1)
     tma_wide_kernel(const __grid_constant__ TmaArgs<kMaxRanks> a)
 {
     using Tr = Traits<T>;
     constexpr int VEC = Tr::VEC;
     constexpr int S_ELEM = (VEC == 8) ? 2 : 4;
+    constexpr uint32_t O = kTmaWideOut;
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int p = a.p;
     const uint32_t TB = a.tile_bytes, S = a.stages, R = a.ranks_per_stage;
     const uint32_t B = (uint32_t(p) + R - 1) / R;                    // stages per tile
     unsigned char *in_base = smem;                                   // [S][R][TB]
-    unsigned char *out_base = smem + size_t(S) * R * TB;             // [2][TB]
-    uint64_t *full = reinterpret_cast<uint64_t *>(out_base + 2 * size_t(TB));
-    uint64_t *empty = full + S;
-    volatile TmaCtl *ctl = reinterpret_cast<volatile TmaCtl *>(empty + S);
+    unsigned char *out_base = smem + size_t(S) * R * TB;             // [O][TB]
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_base + size_t(O) * TB);
+    uint64_t *empty = full + S;        // the 8 consumer warps have read the stage's input slots
+    uint64_t *folded = empty + S;      // the 8 consumer warps have written their parts of out tile o
+    uint64_t *out_free = folded + O;   // the stores of out tile o have read it
+    volatile TmaPipeCtl *ctl = reinterpret_cast<volatile TmaPipeCtl *>(out_free + O);
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), kTmaConsumerWarps);
         }
+        for (uint32_t o = 0; o < O; ++o) {
+            mbar_init(smem_addr(&folded[o]), kTmaConsumerWarps);
+            mbar_init(smem_addr(&out_free[o]), 1);
+        }
         ctl->abort = 0;
-        ctl->go = 0;
         ctl->issued = 0;
-        ctl->consumed = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async_smem();
     }
@@ -655,19 +501,57 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 }
             }
         }
+    } else if (warp == 1) {
+        // ------------------------------ store warp ----------------------------
+        if (lane == 0) {
+            int c = 0;
+            for (uint32_t k = 0;; ++k) {
+                const uint32_t o = k % O;
+                if (!bounded_wait(a, ctl, smem_addr(&folded[o]), (k / O) & 1u, 3u, k)) break;
+                const unsigned long long t = ctl->out_of[o];
+                if (t == kNoTile) break;
+                while (t >= a.tstart[c + 1]) ++c;
+                const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
+                const uint64_t off = cb + (t - a.tstart[c]) * TB;
+                const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
+                const uint32_t out_s = smem_addr(out_base + size_t(o) * TB);
+                if constexpr (MODE == MODE_AR) {
+                    for (int r = 0; r < p; ++r) bulk_store(static_cast<char *>(a.dst[r]) + off, out_s, bytes);
+                } else {
+                    bulk_store(static_cast<char *>(a.dst[c]) + (off - cb), out_s, bytes);
+                }
+                bulk_commit();
+                // the stores of tiles up to k-(O-1) have read their out tiles
+                bulk_wait_read(O - 1);
+                if (k + 1 >= O) mbar_arrive(smem_addr(&out_free[(k + 1 - O) % O]));
+            }
+            bulk_wait_all();
+        }
     } else {
-        // ------------------------------ consumers -----------------------------
-        const int tid = threadIdx.x - 32;
+        // ------------------------------ consumer warps ------------------------
+        // As in the narrow kernel: every lane waits itself, and a vote makes
+        // the warp leave together if any lane's wait gave up.
+        const int cw = warp - 2;
+        const int tid = threadIdx.x - 64;
         GroupFold<T, OP> acc[kTmaWideGroups];
         int c = 0;
-        uint32_t k = 0;  // tiles finished (output tile k & 1)
+        uint32_t k = 0;  // tiles finished by this CTA: the next goes to out tile k % O
         for (uint32_t i = 0;; ++i) {
             const uint32_t s = i % S;
-            if (tid == 0) ctl->go = bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, i) ? 1 : 0;
-            consumer_barrier();
-            if (!ctl->go) break;
+            if (!__all_sync(0xffffffffu, bounded_wait(a, ctl, smem_addr(&full[s]), (i / S) & 1u, 1u, i))) break;
             const unsigned long long meta = ctl->tile_of[s];
-            if (meta == kNoTile) break;
+            const uint32_t o = k % O;
+            if (meta == kNoTile) {
+                // no more work: once out tile o is free (its last tile's id
+                // read), tell the store warp through its barrier
+                if (k >= O &&
+                    !__all_sync(0xffffffffu, bounded_wait(a, ctl, smem_addr(&out_free[o]), ((k / O) - 1) & 1u, 4u, k)))
+                    break;
+                if (cw == 0 && lane == 0) ctl->out_of[o] = kNoTile;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&folded[o]));
+                break;
+            }
             const uint64_t t = meta >> 8;
             const uint32_t b = uint32_t(meta & 255u);
             while (t >= a.tstart[c + 1]) ++c;
@@ -688,13 +572,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&empty[s]));  // this stage's input slots are free
-            if (tid == 0) ctl->consumed = i + 1;
             if (b + 1 == B) {
-                // the tile is complete: write it to output tile k & 1, whose
-                // stores from tile k - 2 must have finished reading it
-                const uint32_t out_s = smem_addr(out_base + size_t(k & 1u) * TB);
-                if (tid == 0 && k >= 2) bulk_wait_read(1);
-                consumer_barrier();
+                // the tile is complete: write it to out tile o once the stores
+                // of tile k - O have read it
+                if (k >= O &&
+                    !__all_sync(0xffffffffu, bounded_wait(a, ctl, smem_addr(&out_free[o]), ((k / O) - 1) & 1u, 4u, k)))
+                    break;
+                const uint32_t out_s = smem_addr(out_base + size_t(o) * TB);
 #pragma unroll
                 for (int q = 0; q < kTmaWideGroups; ++q) {
                     const uint32_t g = uint32_t(tid) + uint32_t(q) * kTmaConsumers;
@@ -702,26 +586,22 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                     sts_v4(out_s + g * 16, acc[q].finish(p));
                 }
                 fence_proxy_async_smem();                      // out tile visible to the bulk stores
-                consumer_barrier();
-                if (tid == 0) {
-                    if constexpr (MODE == MODE_AR) {
-                        for (int r = 0; r < p; ++r) bulk_store(static_cast<char *>(a.dst[r]) + off, out_s, bytes);
-                    } else {
-                        bulk_store(static_cast<char *>(a.dst[c]) + (off - cb), out_s, bytes);
-                    }
-                    bulk_commit();
+                __syncwarp();
+                if (lane == 0) {
+                    if (cw == 0) ctl->out_of[o] = t;
+                    mbar_arrive(smem_addr(&folded[o]));        // this warp's part of out tile o is written
                 }
                 ++k;
             }
         }
-        if (tid == 0) bulk_wait_all();
     }
     __syncthreads();
     // After an abort, wait (bounded) for loads still in flight into shared
-    // memory before the CTA gives its shared memory back.
+    // memory -- at most the last S stages issued -- before the CTA gives its
+    // shared memory back.
     if (threadIdx.x == 0 && ctl->abort) {
         const uint32_t issued = ctl->issued;
-        for (uint32_t j = ctl->consumed; j < issued; ++j) {
+        for (uint32_t j = issued > S ? issued - S : 0; j < issued; ++j) {
             const uint32_t bar = smem_addr(&full[j % S]);
             const uint64_t t0 = global_ns();
             while (!mbar_try_wait(bar, (j / S) & 1u))
@@ -749,7 +629,7 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
     TmaArgs<PM> a;
     uint32_t tile = 0, stages = 0;
     size_t smem = 0;
-    if (!tma_geometry(L.p, L.pipe_bytes, &tile, &stages, &smem)) return cudaErrorInvalidValue;
+    if (!tma_geometry(L.p, L.pipe_bytes, L.sm_budget, &tile, &stages, &smem)) return cudaErrorInvalidValue;
     static_assert(sizeof(TmaCtl) <= kTmaNarrowCtlBytes && sizeof(TmaPipeCtl) <= kTmaNarrowCtlBytes, "control block");
     for (int k = 0; k < L.p; ++k) {
         a.src[k] = L.src[k];
@@ -774,15 +654,8 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
     a.wait_ns = L.wait_limit_ns;
     a.stall_test = L.stall_test;
 
-    void (*kern)(const TmaArgs<PM>) = nullptr;
-    int threads = 0;
-    if constexpr (P == 16) {
-        kern = tma_reduce_sync_kernel<T, OP, P, MODE>;
-        threads = kTmaThreads;
-    } else {
-        kern = tma_reduce_kernel<T, OP, P, MODE>;
-        threads = kTmaPipeThreads;
-    }
+    void (*kern)(const TmaArgs<PM>) = tma_reduce_kernel<T, OP, P, MODE>;
+    const int threads = kTmaPipeThreads;
     static std::atomic<unsigned long long> attr{0};  // devices on which the limit is raised
     {
         const cudaError_t err = allow_dynamic_smem(kern, kTmaSmemLimit, L.device, attr);
@@ -845,12 +718,12 @@ static cudaError_t tma_wide_launch(const Launch &L, LaunchInfo *info)
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) cap = uint64_t(L.sm_budget);
     const int grid = int(tiles < cap ? (tiles ? tiles : 1) : cap);
     a.dynamic = L.tile_counter && tiles >= 16ull * uint64_t(grid) ? 1 : 0;  // a tile here is B stages of work
-    cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(kTmaThreads), smem, L.stream, a);
+    cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(kTmaPipeThreads), smem, L.stream, a);
     if (err != cudaSuccess) return err;
     if (info) {
         info->kernel = MODE == MODE_AR ? "allreduce_tma_wide" : "reduce_scatter_tma_wide";
         info->grid = grid;
-        info->block = kTmaThreads;
+        info->block = kTmaPipeThreads;
         info->smem = smem;
         info->kernels = 1;
         info->counter = a.dynamic;
@@ -865,7 +738,6 @@ static cudaError_t tma_launch_op_mode(const Launch &L, LaunchInfo *info)
     case 2: return tma_launch_p<T, OP, 2, MODE>(L, info);
     case 4: return tma_launch_p<T, OP, 4, MODE>(L, info);
     case 8: return tma_launch_p<T, OP, 8, MODE>(L, info);
-    case 16: return tma_launch_p<T, OP, 16, MODE>(L, info);
     default:
         return L.p > kTmaNarrowMaxRanks ? tma_wide_launch<T, OP, MODE>(L, info)
                                         : tma_launch_p<T, OP, 0, MODE>(L, info);

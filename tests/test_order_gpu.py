@@ -12,9 +12,9 @@ the oracle, that each of those mistakes changes the bits on these inputs.
 Every fixed-order path is compared with the oracle bit for bit, under the
 ring, all-pairs and explicit (custom table) schedules: the ld/st kernel for
 the p-specialised instantiations (p = 2, 3, 4, 8, 16), the generic one
-(5, 6, 17, 33, 64) and its other register shapes (fp32 at p = 5/6, fp16/bf16
+(5, 6, 13, 17, 33, 64) and its other register shapes (fp32 at p = 5/6, fp16/bf16
 min/max at p = 8), the SM-budget persistent kernel (with and without its
-work counter), the TMA kernel (narrow, and wide above 32 ranks; static split
+work counter), the TMA kernel (narrow, and wide from 14 ranks; static split
 and tile counter), ReduceScatter through each, the allocation-free entry
 point, the one-phase executor, the stepwise ring (against its own oracle)
 and the fused residual + RMSNorm (its merged residual h).  The ring's order
@@ -48,12 +48,14 @@ def _built():
 # sizes and inputs
 # ---------------------------------------------------------------------------
 
+WIDE_FROM = 14          # the TMA kernel brings the ranks through its stages eight at a time from here
+
+
 def tile_elems(p, dtype):
-    """Elements per TMA tile at the library's default geometry."""
+    """Elements per TMA tile at the library's largest default tile for p (the
+    one a small SM budget takes; on every SM the tile is the same or half)."""
     s = inputs.ELEM_BYTES[dtype]
-    if p > 32:
-        return 8192 // s
-    t = 16384 if p <= 3 else 8192 if p <= 8 else 4096 if p <= 24 else 2048
+    t = 16384 if p <= 4 else 12288 if p <= 6 else 8192
     return t // s
 
 
@@ -61,7 +63,7 @@ def chunk_len(p, dtype):
     """Elements per chunk: several TMA tiles plus a short last one (chunks stay
     16-byte multiples), and at least 66 tiles in all, so that a one-SM budget
     turns on the TMA tile counter."""
-    tiles = max(2 if p > 32 else 3, math.ceil(66 / p))
+    tiles = max(2 if p >= WIDE_FROM else 3, math.ceil(66 / p))
     return tiles * tile_elems(p, dtype) + 24
 
 
@@ -167,7 +169,7 @@ def run_paths(xs, op, dtype, sched, table, paths=PATHS_AR, rs=True):
                 raise AssertionError(f"reduce_scatter {variant}: {desc}") from e
 
 
-P_ALL = [2, 3, 4, 5, 6, 8, 16, 17, 33, 64]
+P_ALL = [2, 3, 4, 5, 6, 8, 13, 16, 17, 33, 64]
 
 
 # ---------------------------------------------------------------------------

@@ -109,14 +109,15 @@ def test_tma_tile_counter_starts_at_zero_for_every_launch():
 
 @pytest.mark.parametrize("dtype,op", [("bf16", "sum"), ("f32", "avg"), ("i32", "prod"), ("f16", "max")])
 def test_tma_wide_ranks_match_oracle(dtype, op):
-    """More than 32 ranks: the wide kernel brings a tile's ranks through the
+    """From 14 ranks: the wide kernel brings a tile's ranks through the
     stages eight at a time and keeps the partial in registers across them;
     bits equal the oracle for AllReduce and ReduceScatter, with a short last
-    tile, a last batch of fewer than eight ranks, several tile sizes and an
-    SM budget."""
+    tile, a last batch of fewer than eight ranks, several tile sizes and SM
+    budgets."""
     s = inputs.ELEM_BYTES[dtype]
     per16 = 16 // s
-    for p, tile, budget in ((33, 0, 0), (40, 4096, 3), (64, 1024, 0), (64, 0, 7)):
+    for p, tile, budget in ((14, 0, 0), (16, 0, 2), (24, 4096, 0), (33, 0, 0), (40, 4096, 3), (64, 1024, 0),
+                            (64, 0, 7)):
         n = p * (3 * 8192 // s + 5 * per16)
         xs = gen(dtype, op, p, n, seed=150 + p)
         storage = inputs.STORAGE[dtype]
@@ -196,9 +197,9 @@ def test_tma_bounded_wait_times_out_and_context_survives(p, budget, tile):
     """The producer withholds a tile (a wait nothing will satisfy); the
     consumers' wait gives up after 20 ms, the kernel records it and returns,
     ccl_comm_check reports CCL_ERR_TIMEOUT once, and the same communicator
-    then runs correctly.  p = 5 and 8 run the kernel whose consumer warps wait
-    on the stage barriers themselves (with its store warp), p = 16 the form
-    with the consumer barrier; one CTA or many."""
+    then runs correctly.  p = 5 and 8 run the narrow kernel (a tile of every
+    rank per stage), p = 16 the wide one (eight ranks per stage); one CTA or
+    many."""
     n = p * (1 << 16)
     xs = gen("bf16", "sum", p, n, seed=45)
     storage = inputs.STORAGE["bf16"]
