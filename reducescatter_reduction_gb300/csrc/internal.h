@@ -74,25 +74,25 @@ constexpr size_t kTmaNarrowCtlBytes = 256;   // pipelined kernels: four barrier 
 // Grids of at most this many CTAs (an SM budget) take larger narrow tiles.
 constexpr int kTmaSmallGrid = 32;
 
-// Default narrow tile.  Each bulk copy costs the SM's copy engine a fixed
-// time (about 50 ns, measured on GB300: under a budget p=8 moves 35 / 65 /
-// 90 / 103 GB/s per SM with 2 / 4 / 6 / 8 KB tiles), so on a few SMs the
-// largest tile that leaves two stages wins; across many SMs more, smaller
-// stages hide DRAM latency better.  Measured (AllReduce, bf16, GB/s per SM at
-// 8-32 SMs; whole-GPU GB/s):
-//   p=2, 3: 16 KB (whole GPU p=2: 7112 vs 6712 with 8 KB; p=3: 7070 vs 6413)
-//   p=4: 16 KB on small grids (95 vs 82 per SM), 8 KB otherwise (76 SMs: 80 vs 75)
-//   p=5: 12 KB (101 vs 80; 76 SMs 85 vs 77; whole GPU within 0.4 %)
-//   p=6: 12 KB on small grids (90 vs 82), 8 KB otherwise (76 SMs: 81 vs 72)
-//   p=7 .. 13: 8 KB (p=12: 99 vs 67 with 4 KB; p=7 with 12 KB: +3 % on 8 SMs, -10 % on 76)
+// Default narrow tile.  Under a budget the kernel's rate per SM rises with
+// the bytes per bulk copy until the SM's port to the crossbar bounds it near
+// 100-105 GB/s; at a given tile, stages of two or three ranks are slower
+// still (measured on GB300, AllReduce, bf16, GB/s per SM at 8 SMs: 8 KB
+// tiles p=2 49, p=4 82, p=8 105; p=2 with 16 / 24 / 32 KB 79 / 103 / 92).
+// Across many SMs more, smaller stages hide DRAM latency better and keep
+// every SM busy on mid-size messages.  Chosen (8-32 SMs; whole GPU):
+//   p=2, 3: 24 KB on small grids (103 and 85 vs 79 and 77 with 16 KB), 16 KB
+//           otherwise (whole GPU p=2: 7112 vs 6712 with 8 KB; 4 MiB per rank:
+//           3816 vs 3357 with 24 KB)
+//   p=4:    12 KB on small grids (105 vs 82 with 8 KB), 8 KB otherwise
+//   p=5:    12 KB (101 vs 80; 76 SMs 85 vs 77; whole GPU within 0.4 %)
+//   p=6:    12 KB on small grids (90 vs 82), 8 KB otherwise (76 SMs: 81 vs 72)
+//   p=7-13: 8 KB (p=12: 99 vs 67 with 4 KB; p=7 with 12 KB: +3 % on 8 SMs, -10 % on 76)
 inline size_t tma_default_tile(int p, int sm_budget)
 {
     const bool small = sm_budget > 0 && sm_budget <= kTmaSmallGrid;
-    if (p <= 3) return 16384;
-    if (p == 4) return small ? 16384 : 8192;
-    if (p == 5) return 12288;
-    if (p == 6) return small ? 12288 : 8192;
-    return 8192;
+    if (small) return p <= 3 ? 24576 : p <= 6 ? 12288 : 8192;
+    return p <= 3 ? 16384 : p == 5 ? 12288 : 8192;
 }
 
 inline bool tma_geometry(int p, size_t want_tile, int sm_budget, uint32_t *tile, uint32_t *stages, size_t *smem)
