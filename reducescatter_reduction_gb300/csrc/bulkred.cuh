@@ -224,6 +224,7 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
     a.wait_ns = L.wait_limit_ns;
     a.stall_test = 0;
     a.ranks_per_stage = ranks;
+    a.grab = 1;  // unused here
 
     auto kern = bulkred_kernel<T, OP, P>;
     static std::atomic<unsigned long long> attr{0};  // devices on which the limit is raised
