@@ -978,6 +978,27 @@ def _threaded_sample(host_slice, total, cores, single_rate, target_s):
     return 2.0 * P * n_t * cores * S * reps / secs / 1e9, n_t, reps, secs
 
 
+def _host_cpu() -> str:
+    """The host CPU's model name (reported beside the oracle timings)."""
+    import platform
+    import subprocess
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline_from(ins):
     """Time the oracle, as it stands, on a slice of the benchmark's own inputs:
     single-threaded on ~10-15 s of work, and on every host core at once (one
@@ -1000,10 +1021,10 @@ def cpu_baseline_from(ins):
                         "one ring AllReduce call on one thread"}
     cores = _host_cores()
     if cores < 2:
-        return {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        return {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu": _host_cpu(),
                 "sample": single["sample"] + f", {secs:.2f} s", "seconds": round(secs, 3)}
     gbs, n_t, reps, tsecs = _threaded_sample(host_slice, ins[0].numel(), cores, rate, 4.0)
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu": _host_cpu(),
             "sample": f"the 2^27-element rank buffers of the benchmark workload split into {cores} disjoint "
                       f"slices of {n_t} elements, one ring AllReduce per slice on its own thread, all at once, "
                       f"{reps} times ({tsecs:.2f} s wall)",
@@ -1054,7 +1075,7 @@ def run_reference(args, dist: Dist):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample": sample, "p": P, "n_per_step": n * cores},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "cpu": _host_cpu(), "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
