@@ -186,6 +186,7 @@ struct TmaPipeCtl {
     uint32_t issued;    // stages whose loads the producer issued
     unsigned long long tile_of[kTmaMaxStages];  // producer -> consumers: the tile in each stage (kNoTile: done)
     unsigned long long out_of[kTmaMaxStages];   // consumers -> store warp: the tile in each out tile
+    unsigned long long unused_grab;             // wide kernel: the grab asked for ahead and never taken
 };
 
 // Bounded wait on an mbarrier phase.  Returns false if the wait gave up
@@ -411,7 +412,8 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
 // 8 consumer warps each waiting for itself), except that the output tiles
 // are not tied to the stages: out tile k % kTmaWideOut holds the CTA's k-th
 // finished tile.  Waits, abort, drain and the tile counter work as in the
-// narrow kernel (one tile per visit: a tile is B stages of work).
+// narrow kernel, with one tile per visit (a tile is B stages of work), or
+// kTmaWideGrab on small grids.
 // ---------------------------------------------------------------------------
 
 constexpr int kTmaWideGroups = 2;  // 16-byte groups per consumer thread per tile (T <= 8 KB)
@@ -514,6 +516,10 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
                     left = G;
                 }
             }
+            // The grab asked for ahead is never taken: storing its value waits
+            // for that atomic to return, so that it has landed before this
+            // CTA counts itself done and the last CTA resets the counter.
+            if (early) ctl->unused_grab = ahead;
             if (!stopped) {
                 // no more work: a stage with no bytes wakes the consumers
                 const uint32_t s = i % S;
@@ -630,9 +636,12 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
                 if (global_ns() - t0 > uint64_t(a.wait_ns)) break;
         }
     }
-    // the last CTA to finish returns the tile counter to zero
+    // The last CTA to finish returns the tile counter to zero; the fence
+    // orders this CTA's counter atomics before its count.
     if (a.dynamic && threadIdx.x == 0) {
+        __threadfence();
         if (atomicAdd(a.status + 6, 1u) == gridDim.x - 1) {
+            __threadfence();
             atomicExch(reinterpret_cast<unsigned long long *>(a.status + 4), 0ull);
             atomicExch(a.status + 6, 0u);
         }

@@ -81,15 +81,18 @@ def test_tma_in_place_and_budgets_equal_ldst(p):
         assert ins.guards_intact()
 
 
-def test_tma_tile_counter_starts_at_zero_for_every_launch():
+@pytest.mark.parametrize("p", [8, 16])
+def test_tma_tile_counter_starts_at_zero_for_every_launch(p):
     """On messages with many tiles per CTA the TMA kernel hands out tiles
     from a counter in the communicator's status block, and the last CTA of a
     launch returns it to zero.  Four launches in a row on one stream (counter
     on 3 SMs, on 2 SMs, the static split on every SM, the counter on 3 SMs
     again), each after its outputs were zeroed on the same stream and with no
     host synchronisation in between: a launch that started from a stale
-    counter would leave zero tiles behind."""
-    p, n = 8, 8 * (3 * 8192 + 40)                  # ragged last tile in every chunk
+    counter would leave zero tiles behind.  p = 16 runs the wide kernel,
+    which on these small grids takes four tiles per visit and asks for its
+    next grab ahead (one grab per CTA is never taken)."""
+    n = p * (3 * 8192 + 40)                        # ragged last tile in every chunk
     xs = gen("f32", "sum", p, n, seed=47)
     ref, _ = run_collective(xs, "ar", "sum", "f32", "ring", variant="ldst")
     ins = RankBuffers(xs, n, np.float32)
@@ -100,6 +103,8 @@ def test_tma_tile_counter_starts_at_zero_for_every_launch():
                 v.zero_()
             ccl.ccl_set_launch(cm.h, budget, "tma", tile)
             ccl.ccl_allreduce(cm.h, "sum", "f32", n, "ring", stream_ptr())
+            if budget:
+                assert "counter=1" in ccl.ccl_comm_last_launch(cm.h)
         torch.cuda.synchronize()
         ccl.ccl_comm_check(cm.h)
     for r in range(p):
