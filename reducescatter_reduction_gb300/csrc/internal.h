@@ -81,9 +81,11 @@ constexpr int kTmaSmallGrid = 32;
 // tiles p=2 49, p=4 82, p=8 105; p=2 with 16 / 24 / 32 KB 79 / 103 / 92).
 // Across many SMs more, smaller stages hide DRAM latency better and keep
 // every SM busy on mid-size messages.  Chosen (8-32 SMs; whole GPU):
-//   p=2, 3: 24 KB on small grids (103 and 85 vs 79 and 77 with 16 KB), 16 KB
-//           otherwise (whole GPU p=2: 7112 vs 6712 with 8 KB; 4 MiB per rank:
-//           3816 vs 3357 with 24 KB)
+//   p=2:    24 KB on small grids (103 vs 79 with 16 KB), 16 KB otherwise
+//           (whole GPU: 7112 vs 6712 with 8 KB; 4 MiB per rank: 3816 vs 3357
+//           with 24 KB)
+//   p=3:    16 KB (small grids: 105, 97 with 24 KB -- through its own
+//           instantiation; the generic one moved 77-85)
 //   p=4:    12 KB on small grids (105 vs 82 with 8 KB), 8 KB otherwise
 //   p=5:    12 KB (101 vs 80; 76 SMs 85 vs 77; whole GPU within 0.4 %)
 //   p=6:    12 KB on small grids (90 vs 82), 8 KB otherwise (76 SMs: 81 vs 72)
@@ -91,7 +93,7 @@ constexpr int kTmaSmallGrid = 32;
 inline size_t tma_default_tile(int p, int sm_budget)
 {
     const bool small = sm_budget > 0 && sm_budget <= kTmaSmallGrid;
-    if (small) return p <= 3 ? 24576 : p <= 6 ? 12288 : 8192;
+    if (small) return p == 2 ? 24576 : p == 3 ? 16384 : p <= 6 ? 12288 : 8192;
     return p <= 3 ? 16384 : p == 5 ? 12288 : 8192;
 }
 

@@ -775,6 +775,7 @@ static cudaError_t tma_launch_op_mode(const Launch &L, LaunchInfo *info)
 {
     switch (L.p) {
     case 2: return tma_launch_p<T, OP, 2, MODE>(L, info);
+    case 3: return tma_launch_p<T, OP, 3, MODE>(L, info);
     case 4: return tma_launch_p<T, OP, 4, MODE>(L, info);
     case 8: return tma_launch_p<T, OP, 8, MODE>(L, info);
     default:
