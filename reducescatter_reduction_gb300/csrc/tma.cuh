@@ -592,10 +592,17 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
             for (int q = 0; q < kTmaWideGroups; ++q) {
                 const uint32_t g = uint32_t(tid) + uint32_t(q) * kTmaConsumers;
                 if (g * 16 >= bytes) continue;
-                for (uint32_t j = 0; j < nb; ++j) {
-                    const uint4 r = lds_v4(in_s + j * TB + g * 16);
-                    if (b == 0 && j == 0) acc[q].first(r, a.scale);
-                    else acc[q].fold(r, a.scale);
+                // the stage's loads in flight before their folds
+                uint4 r[kTmaWideRanks];
+#pragma unroll
+                for (uint32_t j = 0; j < uint32_t(kTmaWideRanks); ++j)
+                    if (j < nb) r[j] = lds_v4(in_s + j * TB + g * 16);
+#pragma unroll
+                for (uint32_t j = 0; j < uint32_t(kTmaWideRanks); ++j) {
+                    if (j < nb) {
+                        if (b == 0 && j == 0) acc[q].first(r[j], a.scale);
+                        else acc[q].fold(r[j], a.scale);
+                    }
                 }
             }
             __syncwarp();
