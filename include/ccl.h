@@ -194,11 +194,12 @@ CCL_API ccl_status_t ccl_comm_set_schedule(ccl_comm_t comm, const uint8_t *order
  *  pipeline_chunk_bytes : 0 = the variant's default (measured per rank
  *              count and, for the TMA kernel, per SM budget).  For the TMA
  *              variants, the bytes per rank moved per pipeline stage
- *              (multiple of 16, 1 KiB .. 32 KiB; at most 8 KiB for the TMA
+ *              (multiple of 16, 1 KiB .. 32 KiB; at most 16 KiB for the TMA
  *              kernel from 14 ranks, which brings the ranks through the
- *              stages eight at a time); a size whose stages do not fit in
- *              shared memory for the communicator's p is refused at the
- *              collective call (CCL_ERR_INVALID_ARG).  The ld/st kernels have no stages
+ *              stages eight at a time, or four above 8 KiB); a size whose
+ *              stages do not fit in shared memory for the communicator's p
+ *              is refused at the collective call (CCL_ERR_INVALID_ARG).  The
+ *              ld/st kernels have no stages
  *              and ignore it.  Results of the fixed-order variants never
  *              depend on it.  This is the stage of the shared-memory pipeline
  *              (T-CCL, "Pipelined Copy and Reduction"), not the multi-MiB

@@ -477,7 +477,7 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
             uint32_t tile, stages;
             size_t smem;
             uint32_t ranks;
-            const bool fits = p > kTmaNarrowMaxRanks ? tma_wide_geometry(p, c->pipe_bytes, &tile, &ranks, &stages, &smem)
+            const bool fits = p > kTmaNarrowMaxRanks ? tma_wide_geometry(p, c->pipe_bytes, sm_budget, &tile, &ranks, &stages, &smem)
                                                      : tma_geometry(p, c->pipe_bytes, sm_budget, &tile, &stages, &smem);
             if (ok && fits) variant = CCL_VARIANT_TMA;
         }
@@ -556,7 +556,7 @@ static ccl_status_t run(ccl_comm *c, int coll, int op, int dtype, size_t n, int 
         size_t smem;
         uint32_t ranks;
         const bool fits = variant == CCL_VARIANT_TMA
-                              ? (p > kTmaNarrowMaxRanks ? tma_wide_geometry(p, c->pipe_bytes, &tile, &ranks, &stages, &smem)
+                              ? (p > kTmaNarrowMaxRanks ? tma_wide_geometry(p, c->pipe_bytes, sm_budget, &tile, &ranks, &stages, &smem)
                                                         : tma_geometry(p, c->pipe_bytes, sm_budget, &tile, &stages, &smem))
                               : bulkred_geometry(p, c->pipe_bytes, &tile, &ranks, &stages, &smem);
         if (!fits)

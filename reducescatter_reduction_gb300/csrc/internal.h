@@ -117,25 +117,33 @@ inline bool tma_geometry(int p, size_t want_tile, int sm_budget, uint32_t *tile,
 
 // Above kTmaNarrowMaxRanks ranks a stage holding one tile of every rank
 // would force tiles below 8 KB (p+1 of them per stage, two stages), and
-// smaller bulk copies cost more per byte.  The wide geometry keeps 8 KB per
-// copy and brings the p ranks through the stages R at a time (a tile takes
-// ceil(p/R) stages); kTmaWideOut output tiles sit beside the stages.  T <=
-// 8 KB so that each consumer thread folds at most two 16-byte groups per tile
-// in registers.  Measured on GB300 (AllReduce, bf16), wide against narrow:
-// p=14 on 16 SMs 84 vs 84 GB/s per SM (6 KB tiles), on 76 SMs 81 vs 77, whole
-// GPU +1 %; p=16 90 vs 78 (4 KB tiles); p=24 93 vs 77; p=32 93 vs 48 (2 KB);
-// p=13 83 vs 99 (narrow, 8 KB tiles) -- so the wide kernel from 14 ranks.
-// More output tiles (3 or 4) measured the same as two.
+// smaller bulk copies cost more per byte.  The wide geometry keeps 8 or
+// 16 KB per copy and brings the p ranks through the stages R at a time (a
+// tile takes ceil(p/R) stages); kTmaWideOut output tiles sit beside the
+// stages.  T <= 16 KB so that each consumer thread folds at most four 16-byte
+// groups per tile in registers.  Measured on GB300 (AllReduce, bf16), wide
+// (8 ranks of 8 KB) against narrow: p=14 on 16 SMs 84 vs 84 GB/s per SM (6 KB
+// tiles), on 76 SMs 81 vs 77, whole GPU +1 %; p=16 90 vs 78 (4 KB tiles); p=24
+// 93 vs 77; p=32 93 vs 48 (2 KB); p=13 83 vs 99 (narrow, 8 KB tiles) -- so
+// the wide kernel from 14 ranks.  Stages of 4 ranks of 16 KB (half the
+// copies per byte) against 8 of 8 KB: on 8-16 SMs p=16 95-96 vs 94, p=24 98-99
+// vs 95, p=64 99 vs 95; on 76 SMs -1 to -3 %, on the whole GPU -0.5 % and up
+// to -7 % at 4-16 MiB per rank -- so 4 x 16 KB on grids of at most
+// kTmaSmallGrid CTAs, 8 x 8 KB otherwise.  More output tiles (3 or 4)
+// measured the same as two.
 constexpr int kTmaNarrowMaxRanks = 13;
-constexpr int kTmaWideRanks = 8;          // R: ranks per stage
+constexpr int kTmaWideRanks = 8;          // the most ranks a stage holds
 constexpr int kTmaWideOut = 2;            // output tiles
+constexpr size_t kTmaWideMaxTile = 16384;
 
-inline bool tma_wide_geometry(int p, size_t want_tile, uint32_t *tile, uint32_t *ranks, uint32_t *stages,
-                              size_t *smem)
+inline bool tma_wide_geometry(int p, size_t want_tile, int sm_budget, uint32_t *tile, uint32_t *ranks,
+                              uint32_t *stages, size_t *smem)
 {
-    const size_t T = want_tile ? want_tile : 8192;
-    if (T > 8192 || T < 1024) return false;
-    const size_t R = size_t(p) < size_t(kTmaWideRanks) ? size_t(p) : size_t(kTmaWideRanks);
+    const bool small = sm_budget > 0 && sm_budget <= kTmaSmallGrid;
+    const size_t T = want_tile ? want_tile : (small ? 16384 : 8192);
+    if (T > kTmaWideMaxTile || T < 1024) return false;
+    const size_t per = T > 8192 ? 4 : size_t(kTmaWideRanks);  // ranks per stage: 64 KB stages at most
+    const size_t R = size_t(p) < per ? size_t(p) : per;
     // out tiles, four barrier arrays (full/empty per stage, folded/out_free per out tile), control block
     const size_t fixed = kTmaWideOut * T + 2 * (kTmaMaxStages + kTmaWideOut) * 8 + kTmaNarrowCtlBytes;
     size_t S = (kTmaSmemLimit - fixed) / (R * T);

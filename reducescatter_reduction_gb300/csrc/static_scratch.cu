@@ -122,7 +122,7 @@ extern "C" ccl_status_t ccl_allreduce_static(int p, void *const *in_ptrs, void *
                     "ccl_allreduce_static: needs 16-byte aligned buffers and chunk boundaries (n=%zu, p=%d)", n, p);
     uint32_t tile, stages, ranks;
     size_t smem;
-    if (!(p > kTmaNarrowMaxRanks ? tma_wide_geometry(p, 0, &tile, &ranks, &stages, &smem)
+    if (!(p > kTmaNarrowMaxRanks ? tma_wide_geometry(p, 0, 0, &tile, &ranks, &stages, &smem)
                                  : tma_geometry(p, 0, 0, &tile, &stages, &smem)))
         return fail(CCL_ERR_UNSUPPORTED, "ccl_allreduce_static: no shared-memory pipeline fits p=%d", p);
     if (n == 0) return CCL_OK;

@@ -55,7 +55,7 @@ def tile_elems(p, dtype):
     """Elements per TMA tile at the library's largest default tile for p (the
     one a small SM budget takes; on every SM the tile is the same or half)."""
     s = inputs.ELEM_BYTES[dtype]
-    t = 24576 if p <= 3 else 12288 if p <= 6 else 8192
+    t = 24576 if p <= 3 else 12288 if p <= 6 else 16384 if p >= WIDE_FROM else 8192
     return t // s
 
 
