@@ -121,8 +121,10 @@ def test_tma_wide_ranks_match_oracle(dtype, op):
     budgets."""
     s = inputs.ELEM_BYTES[dtype]
     per16 = 16 // s
-    for p, tile, budget in ((14, 0, 0), (16, 0, 2), (24, 4096, 0), (33, 0, 0), (40, 4096, 3), (64, 1024, 0),
-                            (64, 0, 7)):
+    # four ranks of a 16 KB tile per stage: the default on small grids (budgets 2 and 7), forced on every SM by
+    # the tile size (40, 16384, 0), and a 12 KB tile (24, 12288, 5); eight ranks of 8 KB or less otherwise
+    for p, tile, budget in ((14, 0, 0), (16, 0, 2), (24, 4096, 0), (24, 12288, 5), (33, 0, 0), (40, 4096, 3),
+                            (40, 16384, 0), (64, 1024, 0), (64, 0, 7)):
         n = p * (3 * 8192 // s + 5 * per16)
         xs = gen(dtype, op, p, n, seed=150 + p)
         storage = inputs.STORAGE[dtype]
