@@ -70,6 +70,9 @@ def parse_args(argv=None):
     ap.add_argument("--rmsnorm-tokens", type=int, default=0,
                     help="profiling mode: only the fused AllReduce + residual + RMSNorm, p=8 bf16, "
                          "[tokens, 8192], warmup + steps calls")
+    ap.add_argument("--ranks", type=int, default=0,
+                    help="profiling: one bf16 AllReduce of this many ranks of --n elements, with --variant and "
+                         "--sm-budget, timed alone")
     ap.add_argument("--moe-rows", type=int, default=0,
                     help="profiling mode: only the p=16 bf16 [rows, 7168] ring AllReduce with --variant and "
                          "--sm-budget, warmup + steps calls")
@@ -1080,6 +1083,40 @@ def run_reference(args, dist: Dist):
     }
 
 
+def run_single(args, dist: Dist, p: int, n: int, mode: dict) -> int:
+    """One bf16 sum AllReduce of p ranks of n elements (N(0,1) inputs, ring),
+    with the chosen variant and SM budget: warm-up, then the timed steps; one
+    JSON line.  The profiling modes (--moe-rows, --ranks) that the summaries
+    in profiles/ name."""
+    import torch
+    import __graft_entry__
+    import reducescatter_reduction_gb300 as ccl
+    __graft_entry__.build()
+    dev = torch.device("cuda", dist.local_rank)
+    ins = [torch.randn(n, device=dev, dtype=torch.float32).to(torch.bfloat16) for _ in range(p)]
+    outs = [torch.empty_like(t) for t in ins]
+    h = ccl.ccl_comm_create(p, [t.data_ptr() for t in ins])
+    ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
+    ccl.ccl_set_launch(h, args.sm_budget, args.variant, 0)
+    s = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s.cuda_stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s.cuda_stream)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / max(1, args.steps)
+    ccl.ccl_comm_check(h)
+    print(json.dumps(dict(mode, variant=args.variant, sm_budget=args.sm_budget, us_per_call=round(us, 2),
+                          GBps=round(2 * p * n * S / (us * 1e-6) / 1e9, 1),
+                          launch=ccl.ccl_comm_last_launch(h))), flush=True)
+    ccl.ccl_comm_destroy(h)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     dist = Dist()
@@ -1114,36 +1151,15 @@ def main(argv=None):
                           "launch": ccl.ccl_comm_last_launch(h)}), flush=True)
         ccl.ccl_comm_destroy(h)
         return 0
-    if args.moe_rows:
-        import torch
-        import __graft_entry__
-        import reducescatter_reduction_gb300 as ccl
-        __graft_entry__.build()
-        dev = torch.device("cuda", dist.local_rank)
-        p, n = 16, args.moe_rows * 7168
-        ins = [torch.randn(n, device=dev, dtype=torch.float32).to(torch.bfloat16) for _ in range(p)]
-        outs = [torch.empty_like(t) for t in ins]
-        h = ccl.ccl_comm_create(p, [t.data_ptr() for t in ins])
-        ccl.ccl_comm_set_outputs(h, [t.data_ptr() for t in outs])
-        ccl.ccl_set_launch(h, args.sm_budget, args.variant, 0)
-        s = torch.cuda.current_stream()
-        for _ in range(args.warmup):
-            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s.cuda_stream)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            ccl.ccl_allreduce(h, "sum", "bf16", n, "ring", s.cuda_stream)
-        e1.record()
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / max(1, args.steps)
-        ccl.ccl_comm_check(h)
-        print(json.dumps({"mode": "moe", "rows": args.moe_rows, "variant": args.variant,
-                          "sm_budget": args.sm_budget, "us_per_call": round(us, 2),
-                          "GBps": round(2 * p * n * S / (us * 1e-6) / 1e9, 1),
-                          "launch": ccl.ccl_comm_last_launch(h)}), flush=True)
-        ccl.ccl_comm_destroy(h)
-        return 0
+    if args.moe_rows or args.ranks:
+        # profiling modes: one AllReduce configuration, timed alone
+        if args.moe_rows:
+            p, n, mode = 16, args.moe_rows * 7168, {"mode": "moe", "rows": args.moe_rows}
+        else:
+            p = args.ranks
+            n = args.n - args.n % (8 * p)          # whole 16-byte groups in every chunk
+            mode = {"mode": "ranks", "p": p, "n": n}
+        return run_single(args, dist, p, n, mode)
     if args.host_buffers:
         import torch
         import __graft_entry__
