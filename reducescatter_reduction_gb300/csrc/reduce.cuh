@@ -112,8 +112,7 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
         for (int k = 0; k < P; ++k) sp[k] = static_cast<const char *>(a.src[a.order[0][k]]);
     }
 
-    auto group = [&](uint64_t g) {
-        const uint64_t e = g * VEC;
+    auto seek = [&](uint64_t e) {
         if (e >= cend) {  // next chunk(s); empty chunks are skipped
             do { ++c; } while (e >= a.bound[c + 1]);
             cend = a.bound[c + 1];
@@ -122,6 +121,10 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
                 for (int k = 0; k < P; ++k) sp[k] = static_cast<const char *>(a.src[a.order[c][k]]);
             }
         }
+    };
+    auto group = [&](uint64_t g) {
+        const uint64_t e = g * VEC;
+        seek(e);
         if (e + VEC > cend) {  // straddles a chunk boundary: per element
             int cj = c;
             for (int j = 0; j < VEC; ++j) {
@@ -166,8 +169,52 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
             st_stream_v4(static_cast<char *>(a.dst[c]) + (e - a.bound[c]) * S, out);
         }
     };
+    // Under an SM budget with p <= 4 each thread takes GB groups at a time
+    // (g0, g0 + step, ...), all loads issued before the first fold, so that
+    // it has eight 16-byte loads in flight as at p = 8 (one group of p loads
+    // left the SM's load queue short: p=2 on 8 SMs moved 86 GB/s per SM,
+    // stalled on its loads).  Each group is folded as by group(): same bits.
+    constexpr int GB = (DYN && P > 0 && P <= 4) ? 8 / P : 1;
+    auto batch = [&](uint64_t g0, uint64_t step) {  // GB groups, all < ngroups
+        if constexpr (GB > 1) {
+            seek(g0 * VEC);
+            if ((g0 + uint64_t(GB - 1) * step) * VEC + VEC > cend) {  // not all in this chunk
+#pragma unroll 1
+                for (int i = 0; i < GB; ++i) group(g0 + uint64_t(i) * step);
+                return;
+            }
+            uint4 r[GB][P > 0 ? P : 1];
+#pragma unroll
+            for (int i = 0; i < GB; ++i)
+#pragma unroll
+                for (int k = 0; k < P; ++k) r[i][k] = ld_in_v4<NC>(sp[k] + (g0 + uint64_t(i) * step) * VEC * S);
+#pragma unroll
+            for (int i = 0; i < GB; ++i) {
+                const uint64_t e = (g0 + uint64_t(i) * step) * VEC;
+                GroupFold<T, OP> acc;
+                acc.first(r[i][0], a.scale);
+#pragma unroll
+                for (int k = 1; k < P; ++k) acc.fold(r[i][k], a.scale);
+                const uint4 out = acc.finish(p);
+                if constexpr (MODE == MODE_AR) {
+#pragma unroll
+                    for (int k = 0; k < P; ++k) st_stream_v4(static_cast<char *>(a.dst[k]) + e * S, out);
+                } else {
+                    st_stream_v4(static_cast<char *>(a.dst[c]) + (e - a.bound[c]) * S, out);
+                }
+            }
+        } else {
+            group(g0);
+        }
+    };
     if (!DYN || !a.dynamic) {
-        for (uint64_t g = tid; g < ngroups; g += stride) group(g);
+        if constexpr (GB > 1) {
+            uint64_t g = tid;
+            for (; g + uint64_t(GB - 1) * stride < ngroups; g += uint64_t(GB) * stride) batch(g, stride);
+            for (; g < ngroups; g += stride) group(g);
+        } else {
+            for (uint64_t g = tid; g < ngroups; g += stride) group(g);
+        }
     } else {
         // Each warp takes blocks of 32 * kWarpGrab consecutive groups: its
         // first statically, the rest from the status block's group counter,
@@ -176,6 +223,7 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
         // p=16 on 90 SMs: 6545 -> 6866 GB/s; p=2 on 76 SMs 5046 -> 5272; no
         // change at 8-32 SMs.
         constexpr int kWarpGrab = 16;
+        static_assert(kWarpGrab % GB == 0, "a warp's block is whole batches");
         const uint32_t lane = threadIdx.x & 31u;
         const uint64_t per = 32ull * kWarpGrab;
         const uint64_t warps = uint64_t(gridDim.x) * (blockDim.x / 32);
@@ -185,9 +233,14 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
             unsigned long long nb = 0;
             if (lane == 0) nb = warps * per + atomicAdd(next, (unsigned long long)per);
 #pragma unroll 1
-            for (int j = 0; j < kWarpGrab; ++j) {
+            for (int j = 0; j < kWarpGrab; j += GB) {
                 const uint64_t g = base + lane + uint64_t(j) * 32;
-                if (g < ngroups) group(g);
+                if (g + uint64_t(GB - 1) * 32 < ngroups) {
+                    batch(g, 32);
+                } else {
+                    for (int i = 0; i < GB; ++i)
+                        if (g + uint64_t(i) * 32 < ngroups) group(g + uint64_t(i) * 32);
+                }
             }
             base = __shfl_sync(0xffffffffu, nb, 0);
         }
