@@ -174,10 +174,11 @@ struct TmaCtl {
 };
 constexpr unsigned long long kNoTile = ~0ull;
 
-// Tiles taken per visit to the tile counter on large messages.  Measured on
-// GB300 (p=8 bf16, 256 MiB per rank, every SM): a static round-robin split
-// reached 6.56 TB/s, one tile per visit 7.03, four 6.95 -- and four is 3-5 %
-// faster than one under SM budgets (p=16 at 16 SMs: 1258 vs 1140 GB/s).
+// Tiles the narrow kernel takes per visit to the tile counter under an SM
+// budget (one on the whole GPU).  Measured on GB300 (p=8 bf16, 256 MiB per
+// rank, every SM): a static round-robin split reached 6.56 TB/s, one tile per
+// visit 7.03, four 6.95 -- and four is 3-5 % faster than one under SM budgets
+// (p=16 at 16 SMs: 1258 vs 1140 GB/s).
 constexpr unsigned kTmaGrab = 4;
 
 // Control words of the narrow kernel (tma_reduce_kernel).
@@ -256,13 +257,13 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
-            // Large messages (a.dynamic): tiles go out kTmaGrab at a time,
+            // Large messages (a.dynamic): tiles go out a.grab at a time,
             // each CTA's first grab statically (tiles blockIdx.x*G ...), the
             // rest from a device-wide counter (the status block's words 4-5),
             // so SMs that run faster take more.  Small messages: tile b, then
             // b + gridDim.x, ... with no counter, which keeps their latency.
             unsigned long long *next = reinterpret_cast<unsigned long long *>(a.status + 4);
-            const unsigned long long G = a.dynamic ? kTmaGrab : 1;
+            const unsigned long long G = a.dynamic ? a.grab : 1;
             int c = 0;
             unsigned long long t = blockIdx.x * G, left = G;   // the current grab: tiles t, t+1, ...
             for (uint32_t i = 0;; ++i) {
@@ -698,7 +699,6 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
     a.wait_ns = L.wait_limit_ns;
     a.stall_test = L.stall_test;
     a.ranks_per_stage = 0;  // wide kernel only
-    a.grab = 1;             // wide kernel only (the narrow kernel takes kTmaGrab tiles per visit)
 
     void (*kern)(const TmaArgs<PM>) = tma_reduce_kernel<T, OP, P, MODE>;
     const int threads = kTmaPipeThreads;
@@ -711,6 +711,11 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
     if (L.sm_budget > 0 && L.sm_budget < L.num_sms) cap = uint64_t(L.sm_budget);
     const int grid = int(tiles < cap ? (tiles ? tiles : 1) : cap);
     // the tile counter pays off once every CTA has many grabs to balance
+    // kTmaGrab tiles per visit to the tile counter under an SM budget, one on
+    // the whole GPU.  Measured on GB300 (AllReduce, bf16, 256 MiB per rank):
+    // whole GPU p=2/4/8/12 6855/6936/6958/6843 -> 6955/7012/7030/6968 GB/s
+    // with one; on 76 SMs one per visit lost 3-16 % at p <= 8.
+    a.grab = (L.sm_budget > 0 && L.sm_budget < L.num_sms) ? kTmaGrab : 1;
     a.dynamic = L.tile_counter && tiles >= 16ull * kTmaGrab * uint64_t(grid) ? 1 : 0;
     cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(threads), smem, L.stream, a);
     if (err != cudaSuccess) return err;
