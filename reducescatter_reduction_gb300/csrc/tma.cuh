@@ -714,9 +714,11 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
     // kTmaGrab tiles per visit to the tile counter under an SM budget, one on
     // the whole GPU.  Measured on GB300 (AllReduce, bf16, 256 MiB per rank):
     // whole GPU p=2/4/8/12 6855/6936/6958/6843 -> 6955/7012/7030/6968 GB/s
-    // with one; on 76 SMs one per visit lost 3-16 % at p <= 8.
+    // with one; on 76 SMs one per visit lost 3-16 % at p <= 8.  The counter
+    // takes over from 16 grabs per CTA (whole GPU, 32-64 MiB per rank: +8 to
+    // +11 % against the static split, which smaller messages keep).
     a.grab = (L.sm_budget > 0 && L.sm_budget < L.num_sms) ? kTmaGrab : 1;
-    a.dynamic = L.tile_counter && tiles >= 16ull * kTmaGrab * uint64_t(grid) ? 1 : 0;
+    a.dynamic = L.tile_counter && tiles >= 16ull * a.grab * uint64_t(grid) ? 1 : 0;
     cudaError_t err = launch_dependent(kern, unsigned(grid), unsigned(threads), smem, L.stream, a);
     if (err != cudaSuccess) return err;
     if (info) {
