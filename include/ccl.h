@@ -114,7 +114,9 @@ typedef enum {
     CCL_ERR_UNSUPPORTED = 2, /* valid request the library does not serve (e.g. bulk-reduce of prod) */
     CCL_ERR_CUDA = 3,        /* a CUDA runtime call failed; ccl_last_error() names it */
     CCL_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (see ccl_comm_check) */
-    CCL_ERR_NOMEM = 5        /* host or device allocation failed */
+    CCL_ERR_NOMEM = 5,       /* host or device allocation failed */
+    CCL_ERR_BOUNDS = 6       /* the checked build saw a kernel compute an access outside a rank
+                                buffer and skipped it (see ccl_bounds_checked); never otherwise */
 } ccl_status_t;
 
 typedef enum { CCL_SUM = 0, CCL_PROD = 1, CCL_MIN = 2, CCL_MAX = 3, CCL_AVG = 4 } ccl_op_t;
@@ -223,8 +225,12 @@ CCL_API ccl_status_t ccl_set_launch(ccl_comm_t comm, int sm_budget, int variant,
  *  stall_test    : 1 makes the TMA producer withhold its second tile, and the
  *                  fused RMSNorm's second CTA of a row withhold its partial
  *                  sum, so that a bounded wait runs out: the timeout path is
- *                  exercised without faulting or hanging the GPU.  0 = off.
- * Errors: CCL_ERR_INVALID_ARG for negative values or stall_test > 1. */
+ *                  exercised without faulting or hanging the GPU.  2 (the
+ *                  checked build only; nothing otherwise) makes the TMA
+ *                  producer's bounds check of its second tile fail, so that
+ *                  the CCL_ERR_BOUNDS path is exercised: the tile's copies
+ *                  are not made.  0 = off.
+ * Errors: CCL_ERR_INVALID_ARG for negative values or stall_test > 2. */
 CCL_API ccl_status_t ccl_comm_set_debug(ccl_comm_t comm, long long wait_limit_ns, int stall_test);
 
 /* Release the communicator and its device status block (no passage of the
@@ -236,9 +242,18 @@ CCL_API ccl_status_t ccl_comm_destroy(ccl_comm_t comm);
 /* Synchronise the communicator's device and read its status block (no
  * passage of the pages: failure detection, housekeeping).
  * CCL_ERR_TIMEOUT if a bounded wait in a kernel gave up since the last
- * check (the block is then cleared), CCL_ERR_CUDA on a CUDA error,
- * otherwise CCL_OK. */
+ * check, CCL_ERR_BOUNDS if (checked build) a kernel computed an access
+ * outside a rank buffer and skipped it -- the block is then cleared --,
+ * CCL_ERR_CUDA on a CUDA error, otherwise CCL_OK. */
 CCL_API ccl_status_t ccl_comm_check(ccl_comm_t comm);
+
+/* 1 if this library is the checked build (compiled with CCL_BOUNDS_CHECK:
+ * every kernel tests the extent of each global access it computes against the
+ * rank buffer it addresses, records the first violation in the status block
+ * and skips the access), 0 for the default build (no passage of the pages:
+ * housekeeping, a test aid; the checked build is slower and is not what the
+ * measurements use). */
+CCL_API int ccl_bounds_checked(void);
 
 /* ---------------------------------------------------------------------------
  * Collectives.  n is always the element count of one full rank buffer.

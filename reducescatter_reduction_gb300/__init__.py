@@ -18,9 +18,11 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libccl.so")
+# CCL_LIBRARY names another build of this library to load instead (the
+# checked build, libccl_checked.so, for tests)
+LIB_PATH = os.environ.get("CCL_LIBRARY") or os.path.join(_HERE, "libccl.so")
 
-CCL_OK, CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED, CCL_ERR_CUDA, CCL_ERR_TIMEOUT, CCL_ERR_NOMEM = range(6)
+CCL_OK, CCL_ERR_INVALID_ARG, CCL_ERR_UNSUPPORTED, CCL_ERR_CUDA, CCL_ERR_TIMEOUT, CCL_ERR_NOMEM, CCL_ERR_BOUNDS = range(7)
 CCL_SUM, CCL_PROD, CCL_MIN, CCL_MAX, CCL_AVG = range(5)
 CCL_F32, CCL_F16, CCL_BF16, CCL_I32 = range(4)
 CCL_SCHED_AUTO, CCL_SCHED_RING, CCL_SCHED_ALLPAIRS, CCL_SCHED_CUSTOM = range(4)
@@ -37,7 +39,7 @@ VARIANTS = {"auto": CCL_VARIANT_AUTO, "ldst": CCL_VARIANT_LDST, "tma": CCL_VARIA
             "one_phase": CCL_VARIANT_ONE_PHASE}
 STATUS_NAMES = {CCL_OK: "CCL_OK", CCL_ERR_INVALID_ARG: "CCL_ERR_INVALID_ARG",
                 CCL_ERR_UNSUPPORTED: "CCL_ERR_UNSUPPORTED", CCL_ERR_CUDA: "CCL_ERR_CUDA",
-                CCL_ERR_TIMEOUT: "CCL_ERR_TIMEOUT", CCL_ERR_NOMEM: "CCL_ERR_NOMEM"}
+                CCL_ERR_TIMEOUT: "CCL_ERR_TIMEOUT", CCL_ERR_NOMEM: "CCL_ERR_NOMEM", CCL_ERR_BOUNDS: "CCL_ERR_BOUNDS"}
 
 # Every symbol include/ccl.h declares.
 EXPORTS = (
@@ -45,7 +47,7 @@ EXPORTS = (
     "ccl_comm_destroy", "ccl_comm_check", "ccl_allreduce", "ccl_reduce_scatter", "ccl_all_gather",
     "ccl_allreduce_static", "ccl_allreduce_static_set_debug", "ccl_allreduce_residual_rmsnorm",
     "ccl_schedule_build", "ccl_schedule_check", "ccl_cost_estimate", "ccl_select_schedule", "ccl_launch_estimate",
-    "ccl_last_error", "ccl_comm_last_launch", "ccl_comm_launch_count", "ccl_version",
+    "ccl_last_error", "ccl_comm_last_launch", "ccl_comm_launch_count", "ccl_version", "ccl_bounds_checked",
 )
 
 
@@ -97,6 +99,7 @@ def load_library(path: str = LIB_PATH):
         "ccl_comm_last_launch": (i, [vp, ctypes.c_char_p, sz]),
         "ccl_comm_launch_count": (u64, [vp]),
         "ccl_version": (i, []),
+        "ccl_bounds_checked": (i, []),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -259,3 +262,8 @@ def ccl_comm_launch_count(comm: int) -> int:
 
 def ccl_version() -> int:
     return load_library().ccl_version()
+
+
+def ccl_bounds_checked() -> bool:
+    """True when the loaded library is the checked build (CCL_BOUNDS_CHECK)."""
+    return bool(load_library().ccl_bounds_checked())

@@ -3,6 +3,11 @@
 Each source in csrc/ is compiled by its own nvcc process (in parallel); the
 objects go to csrc/_build/ and are linked into reducescatter_reduction_gb300/libccl.so.
 Sources whose object is newer than the source and every header are skipped.
+
+build_checked() builds the same sources with CCL_BOUNDS_CHECK defined into
+csrc/_build/checked/ and libccl_checked.so: every kernel then tests the extent
+of each global access it computes against its rank buffer and records a
+violation instead of making the access (a test aid; not built by default).
 """
 from __future__ import annotations
 
@@ -18,6 +23,9 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(CSRC, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libccl.so")
+BUILD_CHECKED = os.path.join(BUILD, "checked")
+LIB_CHECKED = os.path.join(PKG, "libccl_checked.so")
+CHECKED_FLAGS = ["-DCCL_BOUNDS_CHECK=1"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -41,10 +49,10 @@ def _headers():
             + glob.glob(os.path.join(CSRC, "*.inc")) + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def _compile(src: str, extra, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, extra, verbose: bool, build_dir: str = BUILD, cache: bool = True) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     newest_dep = max([os.path.getmtime(src)] + [os.path.getmtime(h) for h in _headers()])
-    if os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep and not extra:
+    if os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep and cache:
         return obj
     cmd = [nvcc()] + NVCC_FLAGS + list(extra) + ["-c", src, "-o", obj + ".tmp"]
     if verbose:
@@ -58,26 +66,35 @@ def _compile(src: str, extra, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every csrc/ source and link libccl.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def _build(build_dir: str, lib: str, flags, cache: bool, force: bool, verbose: bool) -> str:
+    os.makedirs(build_dir, exist_ok=True)
     if force:
-        for o in glob.glob(os.path.join(BUILD, "*.o")):
+        for o in glob.glob(os.path.join(build_dir, "*.o")):
             os.remove(o)
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra_flags, verbose), srcs))
-    if (not os.path.exists(LIB) or force or extra_flags
-            or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs)):
-        tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, flags, verbose, build_dir, cache), srcs))
+    if (not os.path.exists(lib) or force or not cache
+            or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs)):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
         if verbose:
             print(" ".join(cmd), flush=True)
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    """Compile every csrc/ source and link libccl.so; returns its path."""
+    return _build(BUILD, LIB, list(extra_flags), not extra_flags, force, verbose)
+
+
+def build_checked(force: bool = False, verbose: bool = False) -> str:
+    """The checked build (CCL_BOUNDS_CHECK): libccl_checked.so; returns its path."""
+    return _build(BUILD_CHECKED, LIB_CHECKED, CHECKED_FLAGS, True, force, verbose)
 
 
 if __name__ == "__main__":

@@ -127,6 +127,11 @@ __global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
                     break;
                 }
                 const uint32_t nb = uint32_t(p) - b * R < R ? uint32_t(p) - b * R : R;
+                if (!tile_in_bounds(a, cb, ce, off, bytes, kSiteBulkred, t)) {
+                    ctl->abort = 1;
+                    stopped = true;
+                    break;
+                }
                 ctl->tile_of[s] = (t << 8) | b;
                 const uint32_t bar = smem_addr(&full[s]);
                 mbar_arrive_expect_tx(bar, nb * bytes);
@@ -158,6 +163,10 @@ __global__ void __launch_bounds__(kBulkThreads * kBulkMaxPipes)
             const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
             const uint64_t off = cb + (t - a.tstart[c]) * TB;
             const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
+            if (!tile_in_bounds(a, cb, ce, off, bytes, kSiteBulkred, t)) {
+                ctl->abort = 1;
+                break;
+            }
             char *dst = static_cast<char *>(a.dst[c]) + (off - cb);
             const uint32_t nb = uint32_t(p) - b * R < R ? uint32_t(p) - b * R : R;
             const uint32_t slot = smem_addr(in_base + size_t(s) * R * TB);
@@ -225,6 +234,7 @@ static cudaError_t bulkred_launch_p(const Launch &L, LaunchInfo *info)
     a.stall_test = 0;
     a.ranks_per_stage = ranks;
     a.grab = 1;  // unused here
+    a.buf_bytes = uint64_t(L.n) * S_ELEM;
 
     auto kern = bulkred_kernel<T, OP, P>;
     static std::atomic<unsigned long long> attr{0};  // devices on which the limit is raised

@@ -336,7 +336,7 @@ extern "C" ccl_status_t ccl_set_launch(ccl_comm_t c, int sm_budget, int variant,
 extern "C" ccl_status_t ccl_comm_set_debug(ccl_comm_t c, long long wait_limit_ns, int stall_test)
 {
     if (!c) return fail(CCL_ERR_INVALID_ARG, "comm is NULL");
-    if (wait_limit_ns < 0 || stall_test < 0 || stall_test > 1)
+    if (wait_limit_ns < 0 || stall_test < 0 || stall_test > 2)
         return fail(CCL_ERR_INVALID_ARG, "wait_limit_ns %lld / stall_test %d out of range", wait_limit_ns, stall_test);
     c->wait_limit_ns = wait_limit_ns ? wait_limit_ns : 2000000000LL;
     c->stall_test = stall_test;
@@ -367,10 +367,22 @@ extern "C" ccl_status_t ccl_comm_check(ccl_comm_t c)
     if (err != cudaSuccess) return cuda_fail(err, "ccl_comm_check");
     if (st[0] != 0) {
         cudaMemset(c->d_status, 0, 256);
+        if (st[0] == kBoundsCode)
+            return fail(CCL_ERR_BOUNDS, "an access outside a rank buffer was computed and skipped (site %u, block %u, "
+                        "index %u)", st[3], st[1], st[2]);
         return fail(CCL_ERR_TIMEOUT, "a bounded device wait gave up (code %u, block %u, stage %u)", st[0],
                     st[1], st[2]);
     }
     return CCL_OK;
+}
+
+extern "C" int ccl_bounds_checked(void)
+{
+#ifdef CCL_BOUNDS_CHECK
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 extern "C" ccl_status_t ccl_comm_last_launch(ccl_comm_t c, char *buf, size_t len)

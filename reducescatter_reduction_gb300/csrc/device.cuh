@@ -16,6 +16,50 @@
 namespace ccl {
 
 // ---------------------------------------------------------------------------
+// Checked build (compiled with -DCCL_BOUNDS_CHECK; see build.build_checked):
+// before each global access a kernel computes, it tests that the access lies
+// inside the rank buffer it addresses.  A violation records kBoundsCode, the
+// block, the (low 32 bits of the) index and the site in the launch's status
+// block -- the first record wins -- and the access is not made.  The host
+// reports it as CCL_ERR_BOUNDS.  Nothing traps.  In the default build the
+// tests compile away.
+// ---------------------------------------------------------------------------
+#ifdef CCL_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+
+// Sites named in the record (word 3).
+enum BoundsSite : unsigned {
+    kSiteReduceGroup = 1,   // ld/st kernel, a 16-byte group
+    kSiteReduceElem = 2,    // ld/st kernel, one element
+    kSiteTmaLoad = 3,       // TMA kernels, bulk loads of a stage
+    kSiteTmaStore = 4,      // TMA kernels, bulk stores of an out tile
+    kSiteGather = 5,        // AllGather kernel
+    kSiteBulkred = 6,       // bulk-reduce kernel
+};
+
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned *status, unsigned site, uint64_t index)
+{
+    if constexpr (!kBoundsCheck) {
+        (void)ok;
+        (void)status;
+        (void)site;
+        (void)index;
+        return true;
+    } else {
+        if (ok) return true;
+        if (status != nullptr && atomicCAS(&status[0], 0u, kBoundsCode) == 0u) {
+            status[1] = blockIdx.x;
+            status[2] = unsigned(index);
+            status[3] = site;
+        }
+        return false;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Memory access.  Inputs are streamed once: read without allocating in L1,
 // with a 256-byte L2 prefetch hint.  ld_stream_v4 reads through the
 // non-coherent path, which PTX defines only for data that no thread writes

@@ -21,6 +21,8 @@ struct GatherArgs {
     uint64_t nunits;        // p * chunk_units
     int p;
     uint64_t self_mask;     // bit c: dst[c] == src[c], so the owner's chunk is not rewritten
+    uint64_t buf_units;     // units in every rank buffer (checked build: the extent each access is tested against)
+    unsigned *status;       // the communicator's status block (checked build: where a violation is recorded)
 };
 
 template <int U> struct Unit;
@@ -58,6 +60,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             cend = uint64_t(c + 1) * a.chunk_units;
             sc = static_cast<const char *>(a.src[c]);
         }
+        if (!in_bounds(u < a.buf_units && u >= uint64_t(c) * a.chunk_units && c < p, a.status, kSiteGather, u)) continue;
         const auto v = Unit<U>::load(sc + u * U);
         if constexpr (P > 0) {
 #pragma unroll
@@ -84,6 +87,8 @@ static cudaError_t gather_launch(const Launch &L, LaunchInfo *info)
     a.nunits = a.chunk_units * L.p;
     a.p = L.p;
     a.self_mask = L.self_mask;
+    a.buf_units = uint64_t(L.n) * elem_bytes(L.dtype) / U;
+    a.status = L.status;
 
     // the persistent large-CTA kernel only when the message does not already
     // fit in at most `budget` small CTAs

@@ -61,6 +61,10 @@ struct LaunchInfo {
     int counter = 0;           // 1: CTAs or warps took work from a device-wide counter
 };
 
+// Status-block code of an access outside a rank buffer that a kernel of the
+// checked build computed and skipped (device.cuh, in_bounds).
+constexpr unsigned kBoundsCode = 16;
+
 // TMA variant geometry: tile bytes T per rank per stage and the stage count
 // S for p ranks.  A stage holds p input tiles and one output tile; S fills
 // the 227 KB of shared memory one CTA may address (one CTA per SM).  T-CCL

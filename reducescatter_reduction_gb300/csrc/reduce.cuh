@@ -56,6 +56,8 @@ __device__ __forceinline__ void reduce_one(const ReduceArgs<PM> &a, int p, int c
 {
     using Tr = Traits<T>;
     using F = Fold<T, OP>;
+    // every rank buffer holds n elements; chunk c is [bound[c], bound[c+1])
+    if (!in_bounds(e < a.n && e >= a.bound[c] && e < a.bound[c + 1], a.status, kSiteReduceElem, e)) return;
     if constexpr (kSelect16<T, OP>) {
         // min/max of a 16-bit type: keep the chosen input's own bits, as the
         // packed group fold does (the fp32 compare picks the same operand)
@@ -125,6 +127,7 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
     auto group = [&](uint64_t g) {
         const uint64_t e = g * VEC;
         seek(e);
+        if (!in_bounds(e + VEC <= a.n && e >= a.bound[c], a.status, kSiteReduceGroup, e)) return;
         if (e + VEC > cend) {  // straddles a chunk boundary: per element
             int cj = c;
             for (int j = 0; j < VEC; ++j) {
@@ -183,6 +186,8 @@ __device__ __forceinline__ void reduce_body(const ReduceArgs<(P > 0 ? P : kMaxRa
                 for (int i = 0; i < GB; ++i) group(g0 + uint64_t(i) * step);
                 return;
             }
+            const uint64_t elast = (g0 + uint64_t(GB - 1) * step) * VEC;
+            if (!in_bounds(elast + VEC <= a.n && g0 * VEC >= a.bound[c], a.status, kSiteReduceGroup, elast)) return;
             uint4 r[GB][P > 0 ? P : 1];
 #pragma unroll
             for (int i = 0; i < GB; ++i)

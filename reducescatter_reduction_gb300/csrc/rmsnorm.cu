@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
         const uint32_t lbar = uint32_t(__cvta_generic_to_shared(&xbar));
         if (threadIdx.x == 0)
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(lbar), "r"(uint32_t(C * 4)) : "memory");
-        if (int(threadIdx.x) < C && !(a.stall_test && q == 1)) {
+        if (int(threadIdx.x) < C && !(a.stall_test == 1 && q == 1)) {
             const uint32_t k = threadIdx.x;
             const uint32_t raddr = cl_map(uint32_t(__cvta_generic_to_shared(&parts[q])), k);
             const uint32_t rbar = cl_map(lbar, k);

@@ -159,6 +159,11 @@ extern "C" ccl_status_t ccl_allreduce_static(int p, void *const *in_ptrs, void *
     // The record must start at zero for this call.
     err = cudaMemsetAsync(scratch, 0, kStatusBytes, st);
     if (err != cudaSuccess) return cuda_fail(err, "clearing the status record");
+    if (prev[0] == kBoundsCode)
+        return fail(CCL_ERR_BOUNDS,
+                    "ccl_allreduce_static: the previous call computed an access outside a rank buffer and skipped it "
+                    "(site %u, block %u, index %u); its outputs are incomplete",
+                    prev[3], prev[1], prev[2]);
     if (prev[0] != 0)
         return fail(CCL_ERR_TIMEOUT,
                     "ccl_allreduce_static: a bounded device wait of the previous call gave up "

@@ -66,10 +66,11 @@ struct TmaArgs {
     uint32_t stages;            // S
     unsigned *status;           // status block: [0] code, [1] block, [2] tile, [3] role
     long long wait_ns;          // bound on any single wait
-    int stall_test;             // 1: the producer withholds its second tile (timeout test)
+    int stall_test;             // 1: the producer withholds its second tile (timeout test); 2: see tile_in_bounds
     int dynamic;                // 1: tiles beyond each CTA's first grab come from the tile counter
     uint32_t ranks_per_stage;   // wide kernel: R ranks of a tile per stage
     uint32_t grab;              // wide kernel: tiles per visit to the tile counter
+    uint64_t buf_bytes;         // bytes of every rank buffer (checked build: the extent each copy is tested against)
 };
 
 // ---------------------------------------------------------------------------
@@ -190,6 +191,17 @@ struct TmaPipeCtl {
     unsigned long long unused_grab;             // wide kernel: the grab asked for ahead and never taken
 };
 
+// Checked build: a tile's copies, `bytes` at byte offset `off` of chunk
+// [cb, ce), lie inside the chunk and inside every rank buffer.  With
+// stall_test == 2 the producer's check of its second stage reports a
+// violation, so that a test can see the record (the copies are not made).
+template <int PM>
+__device__ __forceinline__ bool tile_in_bounds(const TmaArgs<PM> &a, uint64_t cb, uint64_t ce, uint64_t off,
+                                               uint32_t bytes, unsigned site, uint64_t t, bool forced = false)
+{
+    return in_bounds(!forced && bytes > 0 && off >= cb && off + bytes <= ce && ce <= a.buf_bytes, a.status, site, t);
+}
+
 // Bounded wait on an mbarrier phase.  Returns false if the wait gave up
 // (timeout, recorded in the status block) or another role aborted.
 template <int PM, typename Ctl>
@@ -269,7 +281,7 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
             for (uint32_t i = 0;; ++i) {
                 const uint32_t s = i % S;
                 if (i >= S && !bounded_wait(a, ctl, smem_addr(&empty[s]), ((i / S) - 1) & 1u, 2u, i)) break;
-                if (a.stall_test && i == 1) break;  // withhold this stage: its consumers must time out
+                if (a.stall_test == 1 && i == 1) break;  // withhold this stage: its consumers must time out
                 if (left == 0) {
                     t = a.dynamic ? gridDim.x * G + atomicAdd(next, G) : t + gridDim.x;
                     left = G;
@@ -288,6 +300,10 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
                 const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
                 const uint64_t off = cb + (t - a.tstart[c]) * TB;
                 const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
+                if (!tile_in_bounds(a, cb, ce, off, bytes, kSiteTmaLoad, t, a.stall_test == 2 && i == 1)) {
+                    ctl->abort = 1;
+                    break;
+                }
                 mbar_arrive_expect_tx(bar, uint32_t(p) * bytes);
                 unsigned char *slot = in_base + size_t(s) * p * TB;
                 for (int k = 0; k < p; ++k)
@@ -309,6 +325,10 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
                 const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
                 const uint64_t off = cb + (t - a.tstart[c]) * TB;
                 const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
+                if (!tile_in_bounds(a, cb, ce, off, bytes, kSiteTmaStore, t)) {
+                    ctl->abort = 1;
+                    break;
+                }
                 const uint32_t out_s = smem_addr(out_base + size_t(s) * TB);
                 if constexpr (MODE == MODE_AR) {
                     for (int k = 0; k < p; ++k) bulk_store(static_cast<char *>(a.dst[k]) + off, out_s, bytes);
@@ -495,11 +515,16 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
                         stopped = true;
                         break;
                     }
-                    if (a.stall_test && i == 1) {  // withhold this stage: its consumers must time out
+                    if (a.stall_test == 1 && i == 1) {  // withhold this stage: its consumers must time out
                         stopped = true;
                         break;
                     }
                     const uint32_t nb = uint32_t(p) - b * R < R ? uint32_t(p) - b * R : R;
+                    if (!tile_in_bounds(a, cb, ce, off, bytes, kSiteTmaLoad, t, a.stall_test == 2 && i == 1)) {
+                        ctl->abort = 1;
+                        stopped = true;
+                        break;
+                    }
                     ctl->tile_of[s] = (t << 8) | b;
                     const uint32_t bar = smem_addr(&full[s]);
                     mbar_arrive_expect_tx(bar, nb * bytes);
@@ -549,6 +574,10 @@ __global__ void __launch_bounds__(kTmaPipeThreads, 1)
                 const uint64_t cb = a.bound[c] * S_ELEM, ce = a.bound[c + 1] * S_ELEM;
                 const uint64_t off = cb + (t - a.tstart[c]) * TB;
                 const uint32_t bytes = uint32_t(ce - off < TB ? ce - off : TB);
+                if (!tile_in_bounds(a, cb, ce, off, bytes, kSiteTmaStore, t)) {
+                    ctl->abort = 1;
+                    break;
+                }
                 const uint32_t out_s = smem_addr(out_base + size_t(o) * TB);
                 if constexpr (MODE == MODE_AR) {
                     for (int r = 0; r < p; ++r) bulk_store(static_cast<char *>(a.dst[r]) + off, out_s, bytes);
@@ -698,6 +727,7 @@ static cudaError_t tma_launch_p(const Launch &L, LaunchInfo *info)
     a.status = L.status;
     a.wait_ns = L.wait_limit_ns;
     a.stall_test = L.stall_test;
+    a.buf_bytes = uint64_t(L.n) * S_ELEM;
     a.ranks_per_stage = 0;  // wide kernel only
 
     void (*kern)(const TmaArgs<PM>) = tma_reduce_kernel<T, OP, P, MODE>;
@@ -760,6 +790,7 @@ static cudaError_t tma_wide_launch(const Launch &L, LaunchInfo *info)
     a.status = L.status;
     a.wait_ns = L.wait_limit_ns;
     a.stall_test = L.stall_test;
+    a.buf_bytes = uint64_t(L.n) * S_ELEM;
 
     // devices on which each instantiation's shared-memory limit is raised
     static std::atomic<unsigned long long> attr4{0}, attr8{0};
