@@ -38,6 +38,7 @@ enum BoundsSite : unsigned {
     kSiteTmaStore = 4,      // TMA kernels, bulk stores of an out tile
     kSiteGather = 5,        // AllGather kernel
     kSiteBulkred = 6,       // bulk-reduce kernel
+    kSiteNorm = 7,          // fused AllReduce + residual + RMSNorm
 };
 
 __device__ __forceinline__ bool in_bounds(bool ok, unsigned *status, unsigned site, uint64_t index)

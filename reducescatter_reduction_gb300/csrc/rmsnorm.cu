@@ -162,6 +162,8 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
     if (a.vec) {
         auto pass1 = [&](uint64_t g, uint4 *hk, uint4 *gk) {
             const uint64_t e = base + g * VEC;
+            // rank buffers hold rows * hidden elements, gamma hidden
+            if (!in_bounds(e + VEC <= a.rows * H && (g + 1) * VEC <= H, a.status, kSiteNorm, e)) return;
             if (gk) *gk = *reinterpret_cast<const uint4 *>(static_cast<const char *>(a.gamma) + g * VEC * S);
             int c = 0;
             while (e >= a.bound[c + 1]) ++c;
@@ -221,6 +223,7 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
     } else {
         for (uint64_t j = u0 + threadIdx.x; j < u1; j += blockDim.x) {
             const uint64_t e = base + j;
+            if (!in_bounds(e < a.rows * H && j < H, a.status, kSiteNorm, e)) continue;
             const float y = round_to<T>(fold_one<T>(a, p, e));
             const float h = round_to<T>(__fadd_rn(y, Tr::load1(a.residual, e)));
             Tr::store1(a.residual_out, e, h);
@@ -289,6 +292,7 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
     if (a.vec) {
         auto pass2 = [&](uint64_t g, const uint4 &hq, const uint4 &gq) {
             const uint64_t e = base + g * VEC;
+            if (!in_bounds(e + VEC <= a.rows * H && (g + 1) * VEC <= H, a.status, kSiteNorm, e)) return;
             float h[VEC], gm[VEC];
             Tr::unpack(hq, h);
             Tr::unpack(gq, gm);
@@ -309,12 +313,14 @@ __global__ void __launch_bounds__(THREADS) ar_rmsnorm_kernel(const __grid_consta
         }
         for (uint64_t g = u0 + threadIdx.x + uint64_t(KEEP) * blockDim.x; g < u1; g += blockDim.x) {
             const uint64_t e = base + g * VEC;
+            if (!in_bounds(e + VEC <= a.rows * H && (g + 1) * VEC <= H, a.status, kSiteNorm, e)) continue;
             pass2(g, *reinterpret_cast<const uint4 *>(static_cast<const char *>(a.residual_out) + e * S),
                   *reinterpret_cast<const uint4 *>(static_cast<const char *>(a.gamma) + g * VEC * S));
         }
     } else {
         for (uint64_t j = u0 + threadIdx.x; j < u1; j += blockDim.x) {
             const uint64_t e = base + j;
+            if (!in_bounds(e < a.rows * H && j < H, a.status, kSiteNorm, e)) continue;
             const float o = __fmul_rn(__fmul_rn(Tr::load1(a.residual_out, e), inv), Tr::load1(a.gamma, j));
             for (int k = 0; k < p; ++k) Tr::store1(a.dst[k], e, o);
         }

@@ -1,9 +1,10 @@
 """The checked build (reducescatter_reduction_gb300.build.build_checked:
 every kernel tests each global access it computes against its rank buffer,
 records a violation and skips the access) runs the seeded random cases, the
-order-revealing parity cases of the main kernel paths and the bounds-record
-tests, in a child process that loads libccl_checked.so: every result must
-still equal the oracle's and no violation may be recorded.  This is the
+order-revealing parity cases of the main kernel paths, the fused RMSNorm
+tests and the bounds-record tests, in a child process that loads
+libccl_checked.so: every result must still equal the oracle's and no
+violation may be recorded.  This is the
 race-and-bounds check that stands in for a memory sanitizer."""
 import os
 import subprocess
@@ -30,7 +31,8 @@ def test_checked_build_passes_the_parity_cases():
            os.path.join(HERE, "test_fuzz.py"),
            os.path.join(HERE, "test_fuzz_tma.py"),
            os.path.join(HERE, "test_order_gpu.py") + "::test_sum_order_every_path",
-           os.path.join(HERE, "test_tma.py") + "::test_tma_wide_ranks_match_oracle"]
+           os.path.join(HERE, "test_tma.py") + "::test_tma_wide_ranks_match_oracle",
+           os.path.join(HERE, "test_rmsnorm.py")]
     res = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
     tail = (res.stdout + res.stderr)[-3000:]
     assert res.returncode == 0, tail
