@@ -251,8 +251,7 @@ CCL_API ccl_status_t ccl_comm_check(ccl_comm_t comm);
  * every kernel tests the extent of each global access it computes against the
  * rank buffer it addresses, records the first violation in the status block
  * and skips the access), 0 for the default build (no passage of the pages:
- * housekeeping, a test aid; the checked build is slower and is not what the
- * measurements use). */
+ * housekeeping, a test aid; the measurements use the default build). */
 CCL_API int ccl_bounds_checked(void);
 
 /* ---------------------------------------------------------------------------
